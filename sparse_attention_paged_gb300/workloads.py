@@ -1,0 +1,292 @@
+"""Seeded synthetic inputs for the DSA indexer paged MQA-logits.
+
+This module generates input bytes only.  It holds none of the indexer's
+arithmetic (no dot products, no ReLU, no head weighting, no scaling, no
+masking): it draws random numbers with a CPU ``torch.Generator`` and lays them
+out in the cache formats the pages describe.  The CUDA path and the fp64
+oracle both consume exactly these bytes.
+
+Layouts (per physical page of P = 64 positions, D = 128):
+  * fp8 keys: P*D e4m3 bytes, position-major, then P fp32 scales; one page is
+    8,448 bytes.  "The Dispatch Wire: Connecting a Triton Indexer Kernel to
+    Production Inference", section "The Reasoning and Decision-Making".
+  * bf16 keys: P*D bf16 values, 256 bytes per position, no scale section;
+    one page is 16,384 bytes.  "The Dispatch Decision: Wiring a Triton Kernel
+    into Production", section "The Problem That Led Here".
+
+Value distributions: q ~ N(0,1) rounded to bf16; w ~ N(0,1)/8 in fp32; fp8
+keys are the round-to-nearest-even, saturating e4m3 cast of N(0,1)/s with a
+per-position scale s ~ U[0.5, 2] stored beside them; bf16 keys are N(0,1)
+rounded to bf16.  The five validation shapes printed on "The Final Gate:
+Validating a Custom Triton Indexer Kernel Before Production Deployment",
+section "What the Test Output Reveals", are available as extra decode cases.
+
+Pages that no valid position references are filled with a poison pattern
+(NaN keys and NaN scales) so that a stray read shows up as NaN in the output.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+KV_E4M3 = 0
+KV_BF16 = 1
+H = 64
+D = 128
+P = 64
+FP8_PAGE_BYTES = P * D + P * 4          # 8,448
+FP8_SCALE_OFFSET = P * D                # 8,192
+BF16_PAGE_BYTES = P * D * 2             # 16,384
+POISON_E4M3 = 0x7F                      # e4m3 NaN code
+POISON_BF16 = 0x7FC0                    # bf16 quiet NaN
+POISON_F32 = 0x7FC00000                 # fp32 quiet NaN
+
+
+@dataclass
+class Workload:
+    """One call's worth of inputs, host-resident (numpy)."""
+    name: str
+    kind: str                   # "decode" or "prefill"
+    kv_dtype: int               # KV_E4M3 or KV_BF16
+    R: int                      # rows: requests (decode) or queries (prefill)
+    W: int                      # block-table width in pages
+    q_bits: np.ndarray          # uint16 [R, H, D], bf16 bit patterns
+    w: np.ndarray               # float32 [R, H]
+    kcache: np.ndarray          # uint8 [num_pages * page_stride]
+    page_stride: int            # bytes between consecutive physical pages
+    num_pages: int
+    kscale_offset: int | None   # byte offset of page 0's scales, None = 1.0
+    block_table: np.ndarray     # int32 [rows_bt, W]
+    bt_stride: int              # W, or 0 when all rows share one row
+    seqlens: np.ndarray         # int32 [R]
+    H: int = H
+    D: int = D
+    P: int = P
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def valid_positions(self) -> int:
+        return int(np.clip(self.seqlens.astype(np.int64), 0, self.W * self.P).sum())
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes the method must move (read + write) for one call.
+
+        Keys and scales of every valid position, q and w of every row, the
+        block-table entries of valid pages, the row lengths, and 4 bytes of
+        output for every position of the fixed [R, W*P] output (the -inf fill
+        is part of the contract).  Prefill rows share one block table and one
+        key stream: the keys of the longest row are read once.
+        """
+        per_pos = D + 4 if self.kv_dtype == KV_E4M3 else 2 * D
+        L = np.clip(self.seqlens.astype(np.int64), 0, self.W * self.P)
+        if self.kind == "prefill" and self.bt_stride == 0:
+            key_bytes = int(L.max(initial=0)) * per_pos
+            bt_bytes = int(math.ceil(L.max(initial=0) / self.P)) * 4
+        else:
+            key_bytes = int(L.sum()) * per_pos
+            bt_bytes = int(np.ceil(L / self.P).sum()) * 4
+        row_bytes = self.R * (H * D * 2 + H * 4 + 4)
+        out_bytes = self.R * self.W * self.P * 4
+        return key_bytes + bt_bytes + row_bytes + out_bytes
+
+    def flops(self) -> int:
+        """2*H*D per valid (row, position) pair: the q.k contraction."""
+        return 2 * self.H * self.D * self.valid_positions
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return g
+
+
+def _bf16_bits(x: torch.Tensor) -> np.ndarray:
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _loguniform_int(g: torch.Generator, n: int, lo: int, hi: int) -> torch.Tensor:
+    u = torch.rand(n, generator=g, dtype=torch.float64)
+    v = torch.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))
+    return v.floor().to(torch.int64).clamp(lo, hi)
+
+
+def _fp8_pool(g: torch.Generator, num_pages: int, used: np.ndarray) -> np.ndarray:
+    """Pool of fused fp8 pages; pages listed in `used` get data, others poison."""
+    pool = np.empty((num_pages, FP8_PAGE_BYTES), dtype=np.uint8)
+    pool[:, :FP8_SCALE_OFFSET] = POISON_E4M3
+    pool[:, FP8_SCALE_OFFSET:].view(np.uint32)[:] = POISON_F32
+    n = len(used)
+    if n:
+        s = torch.rand(n, P, generator=g) * 1.5 + 0.5          # U[0.5, 2]
+        x = (torch.randn(n, P, D, generator=g) / s[:, :, None]).clamp(-448.0, 448.0)
+        vals = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        pool[used, :FP8_SCALE_OFFSET] = vals.reshape(n, P * D)
+        pool[used, FP8_SCALE_OFFSET:] = s.numpy().astype(np.float32).view(np.uint8).reshape(n, P * 4)
+    return pool.reshape(-1)
+
+
+def _bf16_pool(g: torch.Generator, num_pages: int, used: np.ndarray) -> np.ndarray:
+    pool = np.empty((num_pages, P * D), dtype=np.uint16)
+    pool[:] = POISON_BF16
+    n = len(used)
+    if n:
+        pool[used] = _bf16_bits(torch.randn(n, P * D, generator=g))
+    return pool.view(np.uint8).reshape(-1)
+
+
+def _rows(g: torch.Generator, R: int) -> tuple[np.ndarray, np.ndarray]:
+    q = _bf16_bits(torch.randn(R, H, D, generator=g))
+    w = (torch.randn(R, H, generator=g) / 8).numpy().astype(np.float32)
+    return q, w
+
+
+def _used_pages(bt: np.ndarray, seqlens: np.ndarray, bt_stride: int) -> np.ndarray:
+    used = []
+    for r in range(len(seqlens)):
+        row = bt[0] if bt_stride == 0 else bt[r]
+        n = int(math.ceil(max(int(seqlens[r]), 0) / P))
+        used.append(row[:min(n, row.shape[0])])
+    if not used:
+        return np.zeros(0, dtype=np.int64)
+    return np.unique(np.concatenate(used)).astype(np.int64)
+
+
+def _assemble(name, kind, kv_dtype, g, W, bt, seqlens, num_pages, bt_stride,
+              R=None, meta=None) -> Workload:
+    R = len(seqlens) if R is None else R
+    used = _used_pages(bt, seqlens, bt_stride)
+    # rows are drawn before the pool so that a row's q/w do not depend on the
+    # pool size
+    q, w = _rows(g, R)
+    if kv_dtype == KV_E4M3:
+        kc, stride, koff = _fp8_pool(g, num_pages, used), FP8_PAGE_BYTES, FP8_SCALE_OFFSET
+    else:
+        kc, stride, koff = _bf16_pool(g, num_pages, used), BF16_PAGE_BYTES, None
+    return Workload(name=name, kind=kind, kv_dtype=kv_dtype, R=R, W=W,
+                    q_bits=q, w=w, kcache=kc, page_stride=stride,
+                    num_pages=num_pages, kscale_offset=koff,
+                    block_table=np.ascontiguousarray(bt, dtype=np.int32),
+                    bt_stride=bt_stride,
+                    seqlens=np.ascontiguousarray(seqlens, dtype=np.int32),
+                    meta=dict(meta or {}))
+
+
+def decode_uniform(name: str, B: int, W: int, max_len: int, pool: int,
+                   seed: int = 0, kv_dtype: int = KV_E4M3) -> Workload:
+    """B requests, L ~ U{1..max_len}, block table = a random permutation of a
+    pool of `pool` pages (first B*W entries), as in the pages' validation."""
+    g = _gen(seed)
+    seqlens = torch.randint(1, max_len + 1, (B,), generator=g).numpy()
+    bt = torch.randperm(pool, generator=g)[: B * W].numpy().reshape(B, W)
+    return _assemble(name, "decode", kv_dtype, g, W, bt, seqlens, pool, W)
+
+
+def decode_loguniform(name: str, B: int, W: int, lo: int, hi: int,
+                      pages_per_req: int, seed: int = 0,
+                      kv_dtype: int = KV_E4M3, seqlens: np.ndarray | None = None,
+                      poison_tail: bool = True) -> Workload:
+    """B requests with L = floor(exp(U[ln lo, ln hi])).  Each request owns
+    `pages_per_req` pages of a shuffled pool; entries past its valid pages
+    point at one poison page (index B*pages_per_req) when `poison_tail`,
+    else at the rest of its own (unreferenced, poisoned) pages."""
+    g = _gen(seed)
+    if seqlens is None:
+        seqlens = _loguniform_int(g, B, lo, hi).numpy()
+    else:
+        _loguniform_int(g, B, lo, hi)         # keep the stream aligned
+    n_data = B * pages_per_req
+    perm = torch.randperm(n_data, generator=g).numpy().reshape(B, pages_per_req)
+    poison = n_data
+    bt = np.full((B, W), poison, dtype=np.int64)
+    for b in range(B):
+        n = int(math.ceil(int(seqlens[b]) / P))
+        if poison_tail:
+            bt[b, :n] = perm[b, :n]
+        else:
+            m = min(W, pages_per_req)
+            bt[b, :m] = perm[b, :m]
+    return _assemble(name, "decode", kv_dtype, g, W, bt, seqlens, n_data + 1, W,
+                     meta={"lo": lo, "hi": hi})
+
+
+def prefill_causal(name: str, n_q: int, W: int, first_limit: int, seed: int = 0,
+                   kv_dtype: int = KV_BF16) -> Workload:
+    """n_q query tokens of one request sharing one block table (a random
+    permutation of W pages); query i may see positions 0..first_limit+i, so
+    its length is first_limit + i + 1."""
+    g = _gen(seed)
+    bt = torch.randperm(W, generator=g).numpy().reshape(1, W)
+    seqlens = (first_limit + 1 + np.arange(n_q)).astype(np.int32)
+    return _assemble(name, "prefill", kv_dtype, g, W, bt, seqlens, W, 0, R=n_q,
+                     meta={"first_limit": first_limit})
+
+
+# ---------------------------------------------------------------------------
+# The named workloads.
+
+def cfg1() -> Workload:
+    """Decode fp8, B=1, W=8, L ~ U{1..512}, pool of 16 pages, seed 0."""
+    g = _gen(0)
+    seqlens = torch.randint(1, 513, (1,), generator=g).numpy()
+    bt = torch.randperm(16, generator=g)[:8].numpy().reshape(1, 8)
+    return _assemble("decode_fp8_B1_W8", "decode", KV_E4M3, g, 8, bt, seqlens, 16, 8)
+
+
+def cfg2a() -> Workload:
+    """Decode fp8, B=16, W=32 (8K-token cap: 2,048 positions), L ~ U{1..2048}."""
+    return decode_uniform("decode_fp8_B16_W32", 16, 32, 2048, 512, seed=0)
+
+
+def cfg2b() -> Workload:
+    """Decode fp8, B=32, W=16, L ~ U{1..1024}."""
+    return decode_uniform("decode_fp8_B32_W16", 32, 16, 1024, 512, seed=0)
+
+
+def cfg3(W: int = 4097) -> Workload:
+    """Decode fp8, B=64, L log-uniform 512..32768; table width W (4097 =
+    262,208 positions uncapped; 512 = the smallest width that holds the
+    same lengths)."""
+    return decode_loguniform(f"decode_fp8_B64_W{W}", 64, W, 512, 32768, 512, seed=0)
+
+
+def cfg3_short(W: int = 4097) -> Workload:
+    """Decode fp8, B=64, L log-uniform 512..2048, width W (4097 vs 32):
+    the same lengths under the uncapped and the 8K-token-capped table."""
+    return decode_loguniform(f"decode_fp8_B64_short_W{W}", 64, W, 512, 2048, 32, seed=1)
+
+
+def cfg4() -> Workload:
+    """Decode bf16, B=64, W=2048, L log-uniform 4096..131072, scale 1."""
+    return decode_loguniform("decode_bf16_B64_W2048", 64, 2048, 4096, 131072, 2048,
+                             seed=0, kv_dtype=KV_BF16, poison_tail=False)
+
+
+def cfg5() -> Workload:
+    """Prefill bf16: 4,096 queries of one request, 352 pages (22,528
+    positions), causal limit of query i = 18432 + i."""
+    return prefill_causal("prefill_bf16_q4096_W352", 4096, 352, 18432, seed=0)
+
+
+def pages_validation_cases() -> list[Workload]:
+    """The five (B, pages, max length) shapes of the pages' validation run,
+    fp8 keys, with a shuffled pool twice the table size."""
+    shapes = [(1, 8, 512), (16, 32, 2048), (32, 16, 1024), (4, 64, 4096), (8, 4, 256)]
+    out = []
+    for i, (B, W, Lmax) in enumerate(shapes):
+        out.append(decode_uniform(f"pages_val_B{B}_W{W}", B, W, Lmax, 2 * B * W, seed=100 + i))
+    return out
+
+
+NAMED = {
+    "1": lambda: [cfg1()],
+    "2": lambda: [cfg2a(), cfg2b()],
+    "3": lambda: [cfg3(4097)],
+    "3ref": lambda: [cfg3(512)],
+    "3short": lambda: [cfg3_short(4097)],
+    "3short_capped": lambda: [cfg3_short(32)],
+    "4": lambda: [cfg4()],
+    "5": lambda: [cfg5()],
+}
