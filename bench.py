@@ -1,0 +1,575 @@
+#!/usr/bin/env python3
+"""Throughput of the DSA indexer paged MQA-logits on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1|2|3|3ref|3short|3short_capped|4|5]
+
+One step is one pass of the indexer over one batch of synthetic inputs (for
+the default workload: the B=16/W=32 and B=32/W=16 fp8 decode batches, two
+library calls).  Inputs are device-resident when the timed region starts;
+K steps run as CUDA-graph replays and are bracketed by a barrier and
+synchronisations, timed with CUDA events on the launching stream.  Input and
+output buffers rotate among enough copies that every step reads HBM, not L2.
+
+Prints one JSON line (rank 0).  `value` is key positions scored per second
+over all ranks (weak scaling: each rank runs the same per-GPU workload).
+`--impl reference` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_paged_gb300 import workloads as wl  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+WORKLOAD_DESC = {
+    "1": "decode fp8 B=1 W=8 L~U[1,512]",
+    "2": "decode fp8 B=16 W=32 L~U[1,2048] + B=32 W=16 L~U[1,1024]",
+    "3": "decode fp8 B=64 W=4097 L log-uniform 512..32768",
+    "3ref": "decode fp8 B=64 W=512 L log-uniform 512..32768",
+    "3short": "decode fp8 B=64 W=4097 L log-uniform 512..2048",
+    "3short_capped": "decode fp8 B=64 W=32 L log-uniform 512..2048",
+    "4": "decode bf16 B=64 W=2048 L log-uniform 4096..131072",
+    "5": "prefill bf16 n_q=4096 W=352 causal limit 18432+i",
+}
+# default (steps, warmup): a timed region of roughly one second per GPU
+DEFAULT_STEPS = {"1": 100000, "2": 100000, "3": 20000, "3ref": 20000, "3short": 40000,
+                 "3short_capped": 100000, "4": 10000, "5": 1000}
+METRIC = "indexer key-positions scored/s & achieved HBM GB/s (frac of roofline), 1 GB300"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="2", choices=sorted(wl.NAMED))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget-s", type=float, default=60.0,
+                    help="host-time budget of the reference (oracle) arm")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+
+        def pick(*names):
+            for n in names:
+                if n in d and isinstance(d[n], (int, float)):
+                    return float(d[n])
+            return None
+        hbm = pick("hbm_gbs", "hbm_GBs", "hbm_copy_gbs")
+        bf = pick("bf16_tflops", "bf16_tflops_burst")
+        bfs = pick("bf16_tflops_sustained")
+        if hbm and bf:
+            return {"hbm_gbs": hbm, "bf16_tflops": bf,
+                    "bf16_tflops_sustained": bfs or bf, "source": "measured"}
+    except (OSError, ValueError):
+        pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS_SUSTAINED, "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_paged_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(f"{kernel}@{workload}")
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.samples.append((time.time(), line.strip()))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        used = inside if inside else rows
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in used:
+            for n, v in zip(names, r[3][5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        out = {"sm_mhz": statistics.median(r[1] for r in used),
+               "sm_max_mhz": max(r[2] for r in used), "reasons": sorted(reasons),
+               "samples": len(used)}
+        if not inside:
+            out["note"] = "timed region shorter than the sampling period; nearest samples"
+        return out
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+class DeviceCall:
+    """One library call with device-resident inputs and its own output."""
+
+    def __init__(self, w: wl.Workload, device):
+        import torch
+        self.w = w
+        self.q = torch.from_numpy(w.q_bits.view(np.int16)).to(device)
+        self.wt = torch.from_numpy(w.w).to(device)
+        self.kcache = torch.from_numpy(w.kcache).to(device)
+        self.bt = torch.from_numpy(w.block_table).to(device)
+        self.seqlens = torch.from_numpy(w.seqlens).to(device)
+        self.out = torch.empty((w.R, w.W * w.P), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.kscale = (None if w.kscale_offset is None
+                       else self.kcache.data_ptr() + w.kscale_offset)
+
+    def nbytes(self):
+        return sum(t.numel() * t.element_size() for t in
+                   (self.q, self.wt, self.kcache, self.bt, self.seqlens, self.out))
+
+    def __call__(self, q=None, wt=None, bt=None, seqlens=None, out=None):
+        import sparse_attention_paged_gb300 as lib
+        w = self.w
+        fn = (lib.dsa_indexer_logits_decode if w.kind == "decode"
+              else lib.dsa_indexer_logits_prefill)
+        out = self.out if out is None else out
+        st = fn(self.q if q is None else q, self.wt if wt is None else wt, self.kcache,
+                self.kscale, w.page_stride, w.num_pages, w.kv_dtype,
+                self.bt if bt is None else bt, w.bt_stride,
+                self.seqlens if seqlens is None else seqlens, w.R, w.H, w.D, w.P, w.W,
+                out, out.stride(0), self.status, None)
+        if st != 0:
+            raise RuntimeError(f"library call failed: {lib.dsa_status_string(st)}")
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from sparse_attention_paged_gb300 import _native
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    _native.load()
+    works = wl.NAMED[args.workload]()
+    step_bytes = sum(w.algorithmic_bytes() for w in works)
+    step_positions = sum(w.valid_positions for w in works)
+    step_flops = sum(w.flops() for w in works)
+    # rotate enough copies that one pass over them exceeds twice the L2
+    copy_bytes = sum(w.algorithmic_bytes() for w in works)
+    n_copies = max(1, min(64, math.ceil(2 * L2_BYTES / max(copy_bytes, 1))))
+    copies = [[DeviceCall(w, device) for w in works] for _ in range(n_copies)]
+    resident = sum(c.nbytes() for cs in copies for c in cs)
+
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
+    Wm = max(3, args.warmup if args.warmup is not None else max(3, K // 100))
+    S = min(K, 500)                           # steps per captured graph
+
+    def capture(n_steps, offset, timing_events=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_steps):
+                cs = copies[(offset + i) % n_copies]
+                for j, c in enumerate(cs):
+                    if timing_events is not None and j == dom_idx:
+                        timing_events[i][0].record()
+                    c()
+                    if timing_events is not None and j == dom_idx:
+                        timing_events[i][1].record()
+        return g
+
+    # the dominant kernel: the call with the largest algorithmic roofline time
+    peaks = read_peaks()
+
+    def roof_time(w):
+        tb = w.algorithmic_bytes() / (peaks["hbm_gbs"] * 1e9)
+        tf = w.flops() / (peaks["bf16_tflops"] * 1e12)
+        return max(tb, tf)
+    dom_idx = max(range(len(works)), key=lambda j: roof_time(works[j]))
+    dom = works[dom_idx]
+
+    # warm-up (untimed), graphs of the same shape as the timed ones
+    for c in [c for cs in copies for c in cs]:
+        c()
+    torch.cuda.synchronize()
+    wg = capture(min(Wm, S), 0)
+    done = 0
+    while done < Wm:
+        wg.replay()
+        done += min(Wm, S)
+    torch.cuda.synchronize()
+
+    # the timed graphs: K = reps * S + rem steps; the dominant call of every
+    # step is bracketed by external timing events inside the graph
+    try:
+        probe = torch.cuda.Event(enable_timing=True, external=True)
+        del probe
+        ext_ok = True
+    except TypeError:
+        ext_ok = False
+    reps, rem = divmod(K, S)
+
+    def ev_pairs(n):
+        return [(torch.cuda.Event(enable_timing=True, external=True),
+                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
+    main_ev = ev_pairs(S) if ext_ok else None
+    rem_ev = ev_pairs(rem) if (ext_ok and rem) else None
+    g_main = capture(S, 0, main_ev)
+    g_rem = capture(rem, (reps * S) % n_copies, rem_ev) if rem else None
+    # one untimed replay of each so that first-replay costs stay outside
+    g_main.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record()
+    dom_ms = []
+    for _ in range(reps):
+        g_main.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    # per-launch durations of the dominant kernel: the events of the last
+    # replay of each graph hold that replay's timestamps
+    if main_ev is not None:
+        dom_ms += [a.elapsed_time(b) for a, b in main_ev]
+    if rem_ev is not None:
+        dom_ms += [a.elapsed_time(b) for a, b in rem_ev]
+    kernel_timing = "events inside the timed graph (last replay)"
+    if not dom_ms:
+        # torch without external events: time the dominant call alone
+        n = min(S, 200)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for i in range(n):
+            evs[i][0].record()
+            copies[i % n_copies][dom_idx]()
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        dom_ms = [a.elapsed_time(b) for a, b in evs]
+        kernel_timing = "events around eager launches of the dominant call"
+
+    # max over ranks
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed_ms = float(t.item())
+
+    # status check: the timed calls raised no data error
+    for cs in copies:
+        for c in cs:
+            if int(c.status.item()) != 0:
+                raise RuntimeError(f"kernel status {int(c.status.item())}")
+
+    value = world * K * step_positions / (elapsed_ms / 1e3)
+    dom_avg_s = statistics.mean(dom_ms) / 1e3
+    if dom.kind == "prefill":
+        achieved = dom.flops() / dom_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
+    else:
+        achieved = dom.algorithmic_bytes() / dom_avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]}
+    kname = "decode" if dom.kind == "decode" else "prefill"
+    roof["traffic"] = recorded_traffic(kname, dom.name)
+    roof["kernel"] = f"{kname} ({dom.name})"
+    roof["algorithmic_bytes_per_launch"] = dom.algorithmic_bytes()
+    roof["flops_per_launch"] = dom.flops()
+    roof["avg_launch_us"] = dom_avg_s * 1e6
+    roof["peak_source"] = f"{peaks['source']} ({'of measured' if peaks['source'] == 'measured' else 'of fallback'})"
+    roof["kernel_timing"] = kernel_timing
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "key-positions/s",
+        "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 keys x bf16 q -> f32" if dom.kv_dtype == wl.KV_E4M3 else "bf16 -> f32",
+        "data": "synthetic (seeded generator; no dataset)",
+        "config": {"workload": WORKLOAD_DESC[args.workload],
+                   "calls_per_step": len(works),
+                   "positions_per_step": step_positions,
+                   "algorithmic_bytes_per_step": step_bytes,
+                   "flops_per_step": step_flops,
+                   "l2": f"inputs and outputs rotate over {n_copies} copies "
+                         f"({resident / 2**20:.0f} MiB resident, > 2x L2)",
+                   "timing": f"CUDA graphs of {S} steps, events on the launching stream",
+                   "parallelism": f"replicas x{world} (requests are independent)"},
+        "gb_per_s": K * step_bytes / (elapsed_ms / 1e3) / 1e9,
+        "roofline": roof,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "gpu_launches": K * len(works),
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(works, device, min(K, 2000))
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(works)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(works, device, n_steps):
+    """The same metric through the public API with host buffers: every step
+    copies its inputs (q, w, block table, lengths) from pinned host memory,
+    runs the calls and reads the logits back to pinned host memory.  The key
+    cache stays resident on the device, as it does in serving."""
+    import torch
+    calls = [DeviceCall(w, device) for w in works]
+    host = []
+    h2d = d2h = 0
+    for c in calls:
+        hq = torch.from_numpy(c.w.q_bits.view(np.int16)).pin_memory()
+        hw = torch.from_numpy(c.w.w).pin_memory()
+        hbt = torch.from_numpy(c.w.block_table).pin_memory()
+        hsl = torch.from_numpy(c.w.seqlens).pin_memory()
+        hout = torch.empty(c.out.shape, dtype=torch.float32).pin_memory()
+        host.append((hq, hw, hbt, hsl, hout))
+        h2d += sum(t.numel() * t.element_size() for t in (hq, hw, hbt, hsl))
+        d2h += hout.numel() * 4
+
+    def step():
+        for c, (hq, hw, hbt, hsl, hout) in zip(calls, host):
+            c.q.copy_(hq, non_blocking=True)
+            c.wt.copy_(hw, non_blocking=True)
+            c.bt.copy_(hbt, non_blocking=True)
+            c.seqlens.copy_(hsl, non_blocking=True)
+            c()
+            hout.copy_(c.out, non_blocking=True)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    pos = sum(w.valid_positions for w in works)
+    return {"value": n_steps * pos / (ms / 1e3), "unit": "key-positions/s",
+            "steps": n_steps, "ms_per_step": ms / n_steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# the fp64 oracle on the host cores
+
+def _page_sample(works, n_pages, seed=0):
+    """Up to n_pages (row, page) units of the workload, each as its own
+    one-page oracle row: returns oracle argument tuples and the positions."""
+    rng = np.random.default_rng(seed)
+    units = []
+    for wi, w in enumerate(works):
+        L = np.clip(w.seqlens.astype(np.int64), 0, w.W * w.P)
+        for r in range(w.R):
+            for p in range(int(math.ceil(L[r] / w.P))):
+                units.append((wi, r, p))
+    if len(units) > n_pages:
+        idx = rng.choice(len(units), n_pages, replace=False)
+        units = [units[i] for i in sorted(idx)]
+    return units
+
+
+def _oracle_units(works, units, nthreads):
+    import oracle
+    pos = 0
+    by_w = {}
+    for wi, r, p in units:
+        by_w.setdefault(wi, []).append((r, p))
+    for wi, lst in by_w.items():
+        w = works[wi]
+        rows = np.array([r for r, _ in lst])
+        pages = np.array([p for _, p in lst])
+        bt_rows = w.block_table[0] if w.bt_stride == 0 else None
+        bt = np.array([(bt_rows if bt_rows is not None else w.block_table[r])[p]
+                       for r, p in lst], dtype=np.int32).reshape(-1, 1)
+        seq = np.clip(w.seqlens[rows].astype(np.int64) - pages * w.P, 0, w.P).astype(np.int32)
+        oracle.logits(w.q_bits[rows], w.w[rows], w.kcache, w.kscale_offset, w.page_stride,
+                      w.num_pages, w.kv_dtype, bt, 1, seq, len(rows), w.H, w.D, w.P, 1,
+                      nthreads=nthreads)
+        pos += int(seq.sum())
+    return pos
+
+
+def cpu_baseline(works, budget_s=15.0):
+    """The oracle as it stands, on the host cores, on a bounded sample."""
+    import oracle
+    cores = oracle.cpu_count()
+    total_units = len(_page_sample(works, 10**12))
+    # calibrate on a small sample, then size the measured sample to the budget
+    cal = _page_sample(works, min(total_units, 4 * cores), seed=1)
+    t0 = time.perf_counter()
+    _oracle_units(works, cal, cores)
+    t_unit = (time.perf_counter() - t0) / max(len(cal), 1)
+    n = int(min(total_units, max(cores, budget_s / max(t_unit, 1e-9))))
+    units = _page_sample(works, n, seed=2)
+    t0 = time.perf_counter()
+    pos = _oracle_units(works, units, cores)
+    dt = time.perf_counter() - t0
+    return {"value": pos / dt, "unit": "key-positions/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(units)} of {total_units} (row, page) units of the workload, "
+                      f"{pos} positions, {dt:.1f} s, fp64 C oracle with {cores} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    works = wl.NAMED[args.workload]()
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
+    Wm = max(3, args.warmup if args.warmup is not None else 3)
+    cores = oracle.cpu_count()
+    total_units = len(_page_sample(works, 10**12))
+    cal = _page_sample(works, min(total_units, 2 * cores), seed=1)
+    t0 = time.perf_counter()
+    _oracle_units(works, cal, cores)
+    t_unit = (time.perf_counter() - t0) / max(len(cal), 1)
+    per_step = int(min(total_units, max(1, args.ref_budget_s / (K + Wm) / max(t_unit, 1e-9))))
+    units = _page_sample(works, per_step, seed=2)
+    for _ in range(Wm):
+        _oracle_units(works, units, cores)
+    t0 = time.perf_counter()
+    pos = 0
+    for _ in range(K):
+        pos += _oracle_units(works, units, cores)
+    dt = time.perf_counter() - t0
+    value = pos / dt
+    sample = (f"each step: {len(units)} of {total_units} (row, page) units of the workload "
+              f"({pos // K} positions), fp64 C oracle, {cores} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "key-positions/s",
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": dt * 1e3 / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded generator; no dataset)",
+            "config": {"workload": WORKLOAD_DESC[args.workload]},
+            "cpu_baseline": {"value": value, "unit": "key-positions/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "key-positions/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+/*
+ * dsa_indexer.h -- C ABI of the GB300 (sm_103a) DSA indexer paged
+ * MQA-logits library, libdsa_indexer.so.
+ *
+ * The operation.  For every row r (a decode request, or a prefill query
+ * token) and every cached key position t in [0, W*64):
+ *
+ *     out[r, t] = scale(t) * sum_{h<64} w[r, h] * max(0, q[r, h, :] . k(t))
+ *                                                      if t <  seqlens[r]
+ *     out[r, t] = -inf                                 if t >= seqlens[r]
+ *
+ * The per-head dot, the ReLU, the per-head weights and the per-position
+ * scale are the ingredients listed on "The Dispatch Wire: Connecting a
+ * Triton Indexer Kernel to Production Inference", section "The Road to This
+ * Message".  The -inf rule is the "inf-pattern" criterion of "The Final Gate:
+ * Validating a Custom Triton Indexer Kernel Before Production Deployment",
+ * section "What the Test Output Reveals".  The output shape is fixed
+ * ([rows, W*64]) and work past seqlens[r] is skipped inside the kernel, so a
+ * call can be captured in a CUDA graph and replayed with new lengths and
+ * block tables: "The Moment the Context-Length Tax Vanished: Committing the
+ * O(actual) Triton Indexer", section "The Commit: Engineering as Narrative".
+ *
+ * The key cache.  Keys live in physical pages of 64 positions x D = 128
+ * values.  Position t of row r is slot (t % 64) of physical page
+ * block_table[r][t / 64] (the page table of "The Final Gate ...", section
+ * "Assumptions and Knowledge Required").  Page p starts at
+ * (char*)kcache + p * page_stride_bytes and holds its 64 key rows
+ * position-major (D values per position, contiguous):
+ *   DSA_KV_FP8_E4M3  OCP e4m3 ("e4m3fn") bytes, 128 bytes per position.  The
+ *                    fused page of "The Dispatch Wire ...", section "The
+ *                    Reasoning and Decision-Making", is 8,448 bytes: 8,192
+ *                    bytes of keys then 64 fp32 scales, i.e.
+ *                    page_stride_bytes = 8448 and kscale = kcache + 8192.
+ *   DSA_KV_BF16      bf16, 256 bytes per position, 16,384 bytes per page,
+ *                    no quantisation ("The Dispatch Decision: Wiring a Triton
+ *                    Kernel into Production", section "The Problem That Led
+ *                    Here"); pass kscale = NULL for scale 1.
+ * kscale, when not NULL, is the address of page 0's 64 fp32 scales; page p's
+ * are at (char*)kscale + p * page_stride_bytes.  NULL means scale(t) = 1.
+ *
+ * Common rules for both entry points.
+ *   Memory.   Every pointer except `stream` is a DEVICE pointer owned by the
+ *             caller.  The library allocates nothing, never synchronises and
+ *             launches exactly one kernel per call on `stream` (a
+ *             cudaStream_t; NULL = legacy default stream).  All calls are
+ *             legal inside stream capture.
+ *   Shapes.   Only H = 64, D = 128 and page_size = 64 are supported
+ *             (DSA_ERR_UNSUPPORTED otherwise).  W >= 1.  Rows may be 0 (no
+ *             launch, DSA_OK).
+ *   Layouts.  q: bf16 [rows, 64, 128] contiguous.  w: fp32 [rows, 64]
+ *             contiguous.  block_table: int32, row r at
+ *             block_table + r * bt_stride, W entries used (bt_stride = 0
+ *             means every row shares row 0; otherwise bt_stride >= W).
+ *             seqlens: int32 [rows].  out: fp32, row r at
+ *             out + r * out_stride, W*64 entries written (out_stride >=
+ *             W*64).
+ *   Alignment. q, kcache and out 16-byte aligned; kscale 16-byte aligned;
+ *             page_stride_bytes a multiple of 16 and at least the key bytes
+ *             of a page (8,192 fp8, 16,384 bf16); out_stride a multiple of
+ *             4 (DSA_ERR_MISALIGNED otherwise).
+ *   Host errors.  Invalid arguments are reported by the return value and
+ *             nothing is launched.  A launch failure returns DSA_ERR_CUDA.
+ *   Data errors (found by the kernel; never a trap or a fault):
+ *             - seqlens[r] > W*64: the whole row is written NaN, status
+ *               DSA_ERR_BAD_SEQLEN;
+ *             - a block-table entry outside [0, num_pages) that a valid
+ *               position needs: that page's valid positions are NaN, status
+ *               DSA_ERR_BAD_PAGE;
+ *             - an internal wait that does not complete within its bound:
+ *               the affected outputs are NaN, status DSA_ERR_TIMEOUT.
+ *             The status is stored with atomicMax into *dev_status when
+ *             dev_status is not NULL; the library never clears it (zero it
+ *             before the call to read a fresh status).  seqlens[r] <= 0 is
+ *             not an error: the row is all -inf.  Entries of the block table
+ *             at or past ceil(seqlens[r] / 64) are never read.
+ */
+#ifndef DSA_INDEXER_H
+#define DSA_INDEXER_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_INDEXER_ABI_VERSION 1
+
+typedef enum {
+  DSA_KV_FP8_E4M3 = 0,
+  DSA_KV_BF16 = 1
+} dsa_kv_dtype_t;
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,
+  DSA_ERR_UNSUPPORTED = 2,
+  DSA_ERR_MISALIGNED = 3,
+  DSA_ERR_CUDA = 4,
+  DSA_ERR_TIMEOUT = 5,
+  DSA_ERR_BAD_PAGE = 6,
+  DSA_ERR_BAD_SEQLEN = 7
+} dsa_status_t;
+
+/*
+ * Decode: B requests, one query token each.  Row b uses q[b], w[b], block
+ * table row b and length seqlens[b].  The grid is fixed by (B, W) alone, so
+ * the launch does not depend on the lengths: "The Dispatch Wire ...",
+ * section "The Reasoning and Decision-Making" (one program per request and
+ * page, early exit past the request's length).
+ */
+int dsa_indexer_logits_decode(const void* q, const float* w,
+                              const void* kcache, const void* kscale,
+                              long long page_stride_bytes, int num_pages,
+                              int kv_dtype, const int* block_table,
+                              long long bt_stride, const int* seqlens, int B,
+                              int H, int D, int page_size, int W, float* out,
+                              long long out_stride, int* dev_status,
+                              void* stream);
+
+/*
+ * Prefill: n_q query tokens.  Query i uses q[i], w[i], block-table row i
+ * (bt_stride = 0: all queries share row 0, the one-request prefill of "The
+ * Dispatch Decision ...", section "The Problem That Led Here") and length
+ * seqlens[i] = its causal limit + 1.  Keys are read page by page from the
+ * cache: no gathered copy is made.  kv_dtype DSA_KV_BF16 and bt_stride = 0
+ * are supported (DSA_ERR_UNSUPPORTED otherwise).
+ */
+int dsa_indexer_logits_prefill(const void* q, const float* w,
+                               const void* kcache, const void* kscale,
+                               long long page_stride_bytes, int num_pages,
+                               int kv_dtype, const int* block_table,
+                               long long bt_stride, const int* seqlens,
+                               int n_q, int H, int D, int page_size, int W,
+                               float* out, long long out_stride,
+                               int* dev_status, void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* dsa_status_string(int status);
+
+/* DSA_INDEXER_ABI_VERSION of the loaded library. */
+int dsa_indexer_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_INDEXER_H */

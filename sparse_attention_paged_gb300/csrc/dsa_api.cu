@@ -1,0 +1,122 @@
+// dsa_api.cu -- the C ABI declared in include/dsa_indexer.h: argument
+// checks, parameter packing and the single kernel launch of each call.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsa_common.cuh"
+#include "dsa_indexer.h"
+
+namespace dsa {
+cudaError_t launch_rows_simt(const RowsParams& p, cudaStream_t stream);
+}
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Host-side checks shared by both entry points.  Returns DSA_OK and fills
+// `p`, or an error code (nothing is launched on error).
+int check_and_pack(const void* q, const float* w, const void* kcache,
+                   const void* kscale, long long page_stride, int num_pages,
+                   int kv_dtype, const int* block_table, long long bt_stride,
+                   const int* seqlens, int rows, int H, int D, int page_size,
+                   int W, float* out, long long out_stride, int* dev_status,
+                   dsa::RowsParams* p) {
+  if (rows < 0 || W <= 0) return DSA_ERR_INVALID_ARG;
+  if (H != dsa::kHeads || D != dsa::kDim || page_size != dsa::kPage)
+    return DSA_ERR_UNSUPPORTED;
+  if (kv_dtype != DSA_KV_FP8_E4M3 && kv_dtype != DSA_KV_BF16)
+    return DSA_ERR_INVALID_ARG;
+  if (rows > 0 && (!q || !w || !kcache || !block_table || !seqlens || !out))
+    return DSA_ERR_INVALID_ARG;
+  if (num_pages <= 0) return DSA_ERR_INVALID_ARG;
+  const long long key_bytes =
+      (long long)dsa::kPage * dsa::kDim * (kv_dtype == DSA_KV_BF16 ? 2 : 1);
+  if (page_stride < key_bytes) return DSA_ERR_INVALID_ARG;
+  if (bt_stride != 0 && bt_stride < W) return DSA_ERR_INVALID_ARG;
+  if (bt_stride < 0) return DSA_ERR_INVALID_ARG;
+  if (out_stride < (long long)W * dsa::kPage) return DSA_ERR_INVALID_ARG;
+  if (page_stride % 16 != 0 || out_stride % 4 != 0) return DSA_ERR_MISALIGNED;
+  if (!aligned(q, 16) || !aligned(kcache, 16) || !aligned(out, 16) ||
+      !aligned(w, 4) || !aligned(block_table, 4) || !aligned(seqlens, 4))
+    return DSA_ERR_MISALIGNED;
+  if (kscale && !aligned(kscale, 16)) return DSA_ERR_MISALIGNED;
+
+  p->q = static_cast<const uint16_t*>(q);
+  p->w = w;
+  p->kcache = static_cast<const uint8_t*>(kcache);
+  p->kscale = static_cast<const uint8_t*>(kscale);
+  p->page_stride = page_stride;
+  p->num_pages = num_pages;
+  p->kv_dtype = kv_dtype;
+  p->block_table = block_table;
+  p->bt_stride = bt_stride;
+  p->seqlens = seqlens;
+  p->rows = rows;
+  p->W = W;
+  p->out = out;
+  p->out_stride = out_stride;
+  p->status = dev_status;
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsa_indexer_logits_decode(const void* q, const float* w,
+                              const void* kcache, const void* kscale,
+                              long long page_stride_bytes, int num_pages,
+                              int kv_dtype, const int* block_table,
+                              long long bt_stride, const int* seqlens, int B,
+                              int H, int D, int page_size, int W, float* out,
+                              long long out_stride, int* dev_status,
+                              void* stream) {
+  dsa::RowsParams p;
+  int st = check_and_pack(q, w, kcache, kscale, page_stride_bytes, num_pages,
+                          kv_dtype, block_table, bt_stride, seqlens, B, H, D,
+                          page_size, W, out, out_stride, dev_status, &p);
+  if (st != DSA_OK) return st;
+  if (B == 0) return DSA_OK;
+  cudaError_t e = dsa::launch_rows_simt(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_indexer_logits_prefill(const void* q, const float* w,
+                               const void* kcache, const void* kscale,
+                               long long page_stride_bytes, int num_pages,
+                               int kv_dtype, const int* block_table,
+                               long long bt_stride, const int* seqlens,
+                               int n_q, int H, int D, int page_size, int W,
+                               float* out, long long out_stride,
+                               int* dev_status, void* stream) {
+  dsa::RowsParams p;
+  int st = check_and_pack(q, w, kcache, kscale, page_stride_bytes, num_pages,
+                          kv_dtype, block_table, bt_stride, seqlens, n_q, H, D,
+                          page_size, W, out, out_stride, dev_status, &p);
+  if (st != DSA_OK) return st;
+  if (kv_dtype != DSA_KV_BF16 || bt_stride != 0) return DSA_ERR_UNSUPPORTED;
+  if (n_q == 0) return DSA_OK;
+  cudaError_t e = dsa::launch_rows_simt(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG: invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED: unsupported shape or mode";
+    case DSA_ERR_MISALIGNED: return "DSA_ERR_MISALIGNED: pointer or stride misaligned";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA: CUDA launch failed";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT: a device wait exceeded its bound";
+    case DSA_ERR_BAD_PAGE: return "DSA_ERR_BAD_PAGE: block-table entry outside the pool";
+    case DSA_ERR_BAD_SEQLEN: return "DSA_ERR_BAD_SEQLEN: length exceeds the block table";
+    default: return "unknown dsa status";
+  }
+}
+
+int dsa_indexer_abi_version(void) { return DSA_INDEXER_ABI_VERSION; }
+
+}  // extern "C"

@@ -184,6 +184,18 @@ def decode_uniform(name: str, B: int, W: int, max_len: int, pool: int,
     return _assemble(name, "decode", kv_dtype, g, W, bt, seqlens, pool, W)
 
 
+def decode_with_lengths(name: str, lengths, W: int, seed: int = 0,
+                        kv_dtype: int = KV_E4M3, pool: int | None = None) -> Workload:
+    """Requests with the given lengths; the block table is a random
+    permutation of a pool of `pool` pages (default len(lengths) * W)."""
+    g = _gen(seed)
+    seqlens = np.asarray(lengths, dtype=np.int64)
+    B = len(seqlens)
+    pool = B * W if pool is None else pool
+    bt = torch.randperm(pool, generator=g)[: B * W].numpy().reshape(B, W)
+    return _assemble(name, "decode", kv_dtype, g, W, bt, seqlens, pool, W)
+
+
 def decode_loguniform(name: str, B: int, W: int, lo: int, hi: int,
                       pages_per_req: int, seed: int = 0,
                       kv_dtype: int = KV_E4M3, seqlens: np.ndarray | None = None,

@@ -1,0 +1,92 @@
+"""The C ABI on the host (no GPU needed): the library builds for sm_103a,
+loads, exports every function include/dsa_indexer.h declares, and rejects
+bad arguments before launching anything."""
+import os
+import re
+import shutil
+
+import pytest
+
+from sparse_attention_paged_gb300 import _native
+
+HEADER = os.path.join(_native.INCLUDE, "dsa_indexer.h")
+
+needs_nvcc = pytest.mark.skipif(shutil.which(_native.NVCC) is None and
+                                not os.path.exists(_native.LIB_PATH),
+                                reason="nvcc not available and library not built")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _native.load()
+
+
+@needs_nvcc
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(_native.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+@needs_nvcc
+def test_abi_version_and_status_strings(lib):
+    import sparse_attention_paged_gb300 as s
+    assert s.dsa_indexer_abi_version() == 1
+    for code, name in s.STATUS.items():
+        assert s.dsa_status_string(code).startswith(name)
+    assert "unknown" in s.dsa_status_string(99)
+
+
+# Fake, suitably aligned device addresses: every call below must fail its
+# host-side checks, so nothing is dereferenced or launched.
+A = 0x10000
+
+
+def call(fn="decode", **kw):
+    import sparse_attention_paged_gb300 as s
+    args = dict(q=A, w=A, kcache=A, kscale=A + 8192, page_stride_bytes=8448, num_pages=16,
+                kv_dtype=0, block_table=A, bt_stride=8, seqlens=A, B=1, H=64, D=128,
+                page_size=64, W=8, out=A, out_stride=512, dev_status=None, stream=0)
+    args.update(kw)
+    if fn == "prefill":
+        args["n_q"] = args.pop("B")
+        return s.dsa_indexer_logits_prefill(**args)
+    return s.dsa_indexer_logits_decode(**args)
+
+
+@needs_nvcc
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=32), 2), (dict(D=64), 2), (dict(page_size=32), 2),
+    (dict(W=0), 1), (dict(B=-1), 1), (dict(kv_dtype=2), 1),
+    (dict(q=None), 1), (dict(out=None), 1), (dict(block_table=None), 1),
+    (dict(seqlens=None), 1), (dict(w=None), 1), (dict(kcache=None), 1),
+    (dict(num_pages=0), 1), (dict(page_stride_bytes=4096), 1),
+    (dict(bt_stride=3), 1), (dict(out_stride=100), 1),
+    (dict(page_stride_bytes=8456), 3), (dict(out_stride=514), 3),
+    (dict(q=A + 8), 3), (dict(kcache=A + 4), 3), (dict(out=A + 4), 3),
+    (dict(kscale=A + 8196), 3),
+    (dict(kv_dtype=1, page_stride_bytes=8448), 1),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    assert call(**kw) == code
+
+
+@needs_nvcc
+def test_zero_rows_returns_ok_without_launch(lib):
+    assert call(B=0) == 0
+
+
+@needs_nvcc
+def test_prefill_mode_checks(lib):
+    assert call("prefill", kv_dtype=0, bt_stride=0) == 2                     # fp8 prefill
+    assert call("prefill", kv_dtype=1, page_stride_bytes=16384, kscale=None,
+                bt_stride=8) == 2                                             # per-query tables
+    assert call("prefill", kv_dtype=1, page_stride_bytes=16384, kscale=None,
+                bt_stride=0, B=0) == 0

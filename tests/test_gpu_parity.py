@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the fp64
+oracle on the same seeded bytes.  The -inf mask must agree exactly and the
+finite logits within max|d| <= 1e-3 * max|logit| (per call)."""
+import numpy as np
+import pytest
+
+from sparse_attention_paged_gb300 import workloads as wl
+from tests.parity import DeviceWorkload, compare, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    from sparse_attention_paged_gb300 import _native
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    _native.build()
+    yield
+
+
+def _run(w, **kw):
+    import torch
+    dw = DeviceWorkload(w)
+    st = dw.call(**kw)
+    assert st == 0, st
+    torch.cuda.synchronize()
+    return dw
+
+
+def _check_full(w):
+    dw = _run(w)
+    assert int(dw.status.item()) == 0
+    ref, st = oracle_rows(w)
+    assert st == 0
+    return compare(dw.out.cpu().numpy(), ref)
+
+
+# --- the small decode configurations, several seeds ----------------------
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("shape", [(1, 8, 512, 16), (16, 32, 2048, 512), (32, 16, 1024, 512)],
+                         ids=["B1_W8", "B16_W32", "B32_W16"])
+def test_decode_fp8_small(shape, seed):
+    B, W, Lmax, pool = shape
+    _check_full(wl.decode_uniform(f"s{seed}", B, W, Lmax, pool, seed=seed))
+
+
+def test_named_config_1_and_2():
+    for w in [wl.cfg1(), wl.cfg2a(), wl.cfg2b()]:
+        _check_full(w)
+
+
+@pytest.mark.parametrize("idx", range(5))
+def test_pages_validation_shapes(idx):
+    _check_full(wl.pages_validation_cases()[idx])
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_decode_bf16_small(seed):
+    _check_full(wl.decode_uniform(f"bf{seed}", 8, 12, 12 * 64, 200, seed=seed,
+                                  kv_dtype=wl.KV_BF16))
+
+
+# --- edges ------------------------------------------------------------------
+
+@pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
+def test_edge_lengths(kv):
+    W = 5
+    T = W * 64
+    lengths = [0, 1, 63, 64, 65, 127, 128, 129, T - 1, T, -3, 200]
+    _check_full(wl.decode_with_lengths("edges", lengths, W, seed=3, kv_dtype=kv))
+
+
+@pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
+def test_single_page_table(kv):
+    _check_full(wl.decode_with_lengths("w1", [1, 17, 64, 0, 33], 1, seed=4, kv_dtype=kv))
+
+
+def test_zero_rows_is_a_no_op():
+    import torch
+    import sparse_attention_paged_gb300 as lib
+    w = wl.cfg1()
+    dw = DeviceWorkload(w)
+    dw.out.fill_(7.0)
+    st = lib.dsa_indexer_logits_decode(dw.q, dw.wt, dw.kcache, dw.kscale_ptr, w.page_stride,
+                                       w.num_pages, w.kv_dtype, dw.bt, w.bt_stride, dw.seqlens,
+                                       0, 64, 128, 64, w.W, dw.out, dw.out.stride(0), None, None)
+    torch.cuda.synchronize()
+    assert st == 0 and bool((dw.out == 7.0).all())
+
+
+def test_strided_output_and_table():
+    """out_stride > W*64 and bt_stride > W: padding is left untouched."""
+    import torch
+    w = wl.decode_uniform("strided", 6, 7, 7 * 64, 64, seed=9)
+    ref, _ = oracle_rows(w)
+    dw = DeviceWorkload(w)
+    bt_wide = torch.full((w.R, w.W + 3), -5, dtype=torch.int32, device="cuda")
+    bt_wide[:, : w.W] = dw.bt
+    out_wide = torch.full((w.R, w.W * 64 + 36), 3.0, device="cuda")
+    import sparse_attention_paged_gb300 as lib
+    st = lib.dsa_indexer_logits_decode(dw.q, dw.wt, dw.kcache, dw.kscale_ptr, w.page_stride,
+                                       w.num_pages, w.kv_dtype, bt_wide, w.W + 3, dw.seqlens,
+                                       w.R, 64, 128, 64, w.W, out_wide, out_wide.stride(0),
+                                       dw.status, None)
+    torch.cuda.synchronize()
+    assert st == 0
+    o = out_wide.cpu().numpy()
+    compare(o[:, : w.W * 64], ref)
+    assert (o[:, w.W * 64:] == 3.0).all()
+
+
+# --- data errors: reported in-kernel, never a fault --------------------------
+
+def test_bad_page_id_poisons_its_positions():
+    import torch
+    w = wl.decode_with_lengths("badpage", [150, 70], 3, seed=5)
+    w.block_table = w.block_table.copy()
+    w.block_table[0, 1] = w.num_pages + 11        # needed by row 0 (positions 64..127)
+    w.block_table[1, 2] = -4                      # not needed by row 1 (L = 70)
+    dw = _run(w)
+    assert int(dw.status.item()) == 6
+    ref, st = oracle_rows(w)
+    assert st == 6
+    compare(dw.out.cpu().numpy(), ref)
+
+
+def test_length_past_table_is_a_nan_row():
+    w = wl.decode_with_lengths("badlen", [100, 3 * 64 + 1, 5], 3, seed=6)
+    dw = _run(w)
+    assert int(dw.status.item()) == 7
+    ref, st = oracle_rows(w)
+    assert st == 7
+    o = dw.out.cpu().numpy()
+    assert np.isnan(o[1]).all()
+    compare(o, ref)
+
+
+# --- CUDA graph capture: fixed grid, data-dependent work --------------------
+
+def test_graph_capture_and_replay_with_new_lengths():
+    import torch
+    w0 = wl.decode_uniform("g0", 16, 32, 2048, 512, seed=0)
+    w1 = wl.decode_uniform("g1", 16, 32, 2048, 512, seed=1)
+    dw = DeviceWorkload(w0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dw.call()                                   # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = dw.call()
+    assert st == 0
+    g.replay()
+    torch.cuda.synchronize()
+    compare(dw.out.cpu().numpy(), oracle_rows(w0)[0])
+    # new inputs in the same buffers: lengths, table, q, w and cache all change
+    dw.q.copy_(DeviceWorkload(w1).q)
+    for name in ("wt", "kcache", "bt", "seqlens"):
+        getattr(dw, name).copy_(getattr(DeviceWorkload(w1), name))
+    g.replay()
+    torch.cuda.synchronize()
+    compare(dw.out.cpu().numpy(), oracle_rows(w1)[0])
+
+
+# --- full-size configurations ------------------------------------------------
+
+@pytest.mark.parametrize("W", [4097, 512])
+def test_config3_full(W):
+    stats = _check_full(wl.cfg3(W))
+    assert stats["rel"] < 1e-3
+
+
+@pytest.mark.parametrize("W", [4097, 32])
+def test_config3_short_lengths_capped_and_uncapped(W):
+    _check_full(wl.cfg3_short(W))
+
+
+def test_config3_width_does_not_change_valid_logits():
+    """Same lengths, width 4097 vs 512: identical values below each length
+    (the table's extra entries are never read)."""
+    a = _run(wl.cfg3(4097)).out.cpu().numpy()
+    b = _run(wl.cfg3(512)).out.cpu().numpy()
+    assert np.array_equal(a[:, : 512 * 64], b)
+    assert np.isneginf(a[:, 512 * 64:]).all()
+
+
+def _sampled(w, rows):
+    dw = _run(w)
+    assert int(dw.status.item()) == 0
+    o = dw.out.cpu().numpy()
+    # mask and NaN-freedom on every row, values on the sampled rows
+    T = w.W * w.P
+    L = np.clip(w.seqlens.astype(np.int64), 0, T)
+    assert np.array_equal(np.isneginf(o), np.arange(T)[None, :] >= L[:, None])
+    assert not np.isnan(o).any()
+    ref, st = oracle_rows(w, rows)
+    assert st == 0
+    return compare(o[rows], ref)
+
+
+def test_config4_bf16_full_size_sampled_rows():
+    w = wl.cfg4()
+    L = w.seqlens
+    rows = sorted(set([int(np.argmin(L)), int(np.argmax(L)), 0, 1, 31, 63]))
+    _sampled(w, rows)
+
+
+def test_config5_prefill_full_size_sampled_rows():
+    w = wl.cfg5()
+    rows = [0, 1, 2, 3, 127, 128, 1000, 2047, 2048, 3001, 4094, 4095]
+    _sampled(w, rows)
+
+
+def test_prefill_small_full():
+    _check_full(wl.prefill_causal("pf_small", 70, 9, 9 * 64 - 75, seed=2))
