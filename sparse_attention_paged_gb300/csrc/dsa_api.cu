@@ -7,7 +7,8 @@
 #include "dsa_indexer.h"
 
 namespace dsa {
-cudaError_t launch_rows_simt(const RowsParams& p, cudaStream_t stream);
+cudaError_t launch_decode(const RowsParams& p, cudaStream_t stream);
+cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream);
 }
 
 namespace {
@@ -80,7 +81,8 @@ int dsa_indexer_logits_decode(const void* q, const float* w,
                           page_size, W, out, out_stride, dev_status, &p);
   if (st != DSA_OK) return st;
   if (B == 0) return DSA_OK;
-  cudaError_t e = dsa::launch_rows_simt(p, static_cast<cudaStream_t>(stream));
+  if (B > 65535) return DSA_ERR_UNSUPPORTED;
+  cudaError_t e = dsa::launch_decode(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -99,7 +101,7 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
   if (st != DSA_OK) return st;
   if (kv_dtype != DSA_KV_BF16 || bt_stride != 0) return DSA_ERR_UNSUPPORTED;
   if (n_q == 0) return DSA_OK;
-  cudaError_t e = dsa::launch_rows_simt(p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = dsa::launch_prefill(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

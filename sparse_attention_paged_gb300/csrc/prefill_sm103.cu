@@ -1,0 +1,454 @@
+// prefill_sm103.cu -- prefill kernel of the DSA indexer paged MQA-logits for
+// GB300 (sm_103a): n_q query tokens of one request share one block table;
+// query i may see the positions below its length L_i (causal limit + 1).
+//
+// The keys are read page by page from the paged cache through TMA; no
+// gathered [queries, pages, ...] copy is ever formed ("The Dispatch
+// Decision: Wiring a Triton Kernel into Production", section "The Problem
+// That Led Here": the materialised gather of a 22K-context, 4,096-query
+// prefill is what ran out of memory).
+//
+// Work: items (query tile j of 4 queries, position tile of 128 positions),
+// only for position tiles below the tile's largest length.  A persistent
+// grid of one CTA per SM splits the item list evenly (a block-wide prefix
+// sum over the per-tile lengths), so the causal triangle's skipped tiles cost
+// nothing and every SM gets the same number of MMAs.
+//
+// Per item: tcgen05 MMA with M = 128 positions, N = 256 (4 queries x 64
+// heads), K = 128, f32 accumulator in TMEM, double-buffered (2 x 256
+// columns); 8 epilogue warps (two per TMEM lane quadrant, one query pair
+// each) apply ReLU, the head weights and the position scale and store one
+// coalesced 128-byte row segment per warp and query.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include "dsa_common.cuh"
+#include "sm100_ptx.cuh"
+#include "tensor_maps.cuh"
+
+namespace dsa {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kQT = 4;                        // queries per tile (N = 256)
+constexpr int kN = kQT * kHeads;              // 256
+constexpr int kTileM = 128;                   // positions per tile
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (kEpiWarps + 2) * 32;  // + TMA warp + MMA warp
+constexpr int kABytes = kTileM * kDim * 2;    // 32 KB: 2 K-blocks x 128 rows x 128 B
+constexpr int kBBytes = kN * kDim * 2;        // 64 KB: 2 K-blocks x 256 rows x 128 B
+constexpr int kPageHalf = kPage * 128;        // 8 KB: one page, one K-block
+constexpr int kCtrl = 4096;
+constexpr int kSmem = 1024 + kBBytes + kStages * kABytes + kCtrl;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ float nanf_() { return __int_as_float(0x7fc00000); }
+
+struct Lens {
+  int T;
+  int nq;
+  int nqt;
+  const int* seqlens;
+  // length of query i clamped to [0, T]; an over-long row counts as 0 here
+  // (it is written NaN by the fill)
+  __device__ __forceinline__ int valid(int i) const {
+    if (i >= nq) return 0;
+    const int L = __ldg(seqlens + i);
+    return (L > T) ? 0 : max(L, 0);
+  }
+  // largest valid length among the queries of query tile j
+  __device__ __forceinline__ int lmax(int j) const {
+    int m = 0;
+#pragma unroll
+    for (int q = 0; q < kQT; ++q) m = max(m, valid(kQT * j + q));
+    return m;
+  }
+  __device__ __forceinline__ int tiles(int j) const { return (lmax(j) + kTileM - 1) / kTileM; }
+};
+
+// Walks a CTA's contiguous slice of the item list (query-tile major).
+struct ItemIter {
+  int j, pt, ntl, lmax;
+  const Lens* lens;
+  __device__ void init(const Lens* l, int j0, int pt0) {
+    lens = l;
+    j = j0;
+    pt = pt0;
+    lmax = l->lmax(j0);
+    ntl = (lmax + kTileM - 1) / kTileM;
+  }
+  __device__ void next() {
+    if (++pt < ntl) return;
+    pt = 0;
+    do {
+      if (++j >= lens->nqt) {   // past the end of the list
+        ntl = lmax = 0;
+        return;
+      }
+      lmax = lens->lmax(j);
+      ntl = (lmax + kTileM - 1) / kTileM;
+    } while (ntl == 0);
+  }
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                   const RowsParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sB = smem;
+  uint8_t* sA = smem + kBBytes;
+  uint8_t* ctrl = sA + kStages * kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;   // [2]
+  uint64_t* tempty = tfull + 2;        // [2]
+  uint64_t* bfull = tempty + 2;
+  uint64_t* bempty = bfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 260);
+  int* sm_misc = reinterpret_cast<int*>(ctrl + 272);       // total, start j, start pt
+  float* w_s = reinterpret_cast<float*>(ctrl + 1024);      // [4][64]
+  int* scan = reinterpret_cast<int*>(ctrl + 2048);         // [kThreads]
+  static_assert((2 * kStages + 6) * 8 <= 256, "control block");
+  static_assert(2048 + kThreads * 4 <= kCtrl, "control block");
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.W * kPage;
+  const int n_qt = (p.rows + kQT - 1) / kQT;
+  const Lens lens{T, p.rows, n_qt, p.seqlens};
+  const int P = gridDim.x, k = blockIdx.x;
+  const int* bt = p.block_table;   // shared row (bt_stride == 0)
+
+  // ---- fill: rows of query tiles without any position tile (every length
+  // <= 0, or over-long rows) are written here; the other tiles' tails are
+  // written by the CTA that owns their first item.
+  for (int j = k; j < n_qt; j += P) {
+    if (lens.tiles(j) != 0) continue;
+    for (int q = 0; q < kQT; ++q) {
+      const int i = kQT * j + q;
+      if (i >= p.rows) break;
+      const bool bad = __ldg(p.seqlens + i) > T;
+      const float fv = bad ? nanf_() : -INFINITY;
+      float* orow = p.out + (long long)i * p.out_stride;
+      for (int t = 4 * tid; t < T; t += 4 * kThreads)
+        *reinterpret_cast<float4*>(orow + t) = make_float4(fv, fv, fv, fv);
+      if (bad && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
+    }
+  }
+
+  // ---- this CTA's slice of the item list
+  {
+    const int j0 = (int)((long long)tid * n_qt / kThreads);
+    const int j1 = (int)((long long)(tid + 1) * n_qt / kThreads);
+    int part = 0;
+    for (int j = j0; j < j1; ++j) part += lens.tiles(j);
+    scan[tid] = part;
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0;
+      for (int i = 0; i < kThreads; ++i) {
+        const int v = scan[i];
+        scan[i] = run;
+        run += v;
+      }
+      sm_misc[0] = run;
+      sm_misc[1] = -1;
+    }
+    __syncthreads();
+    const int total = sm_misc[0];
+    const int start = (int)((long long)k * total / P);
+    if (part > 0 && start >= scan[tid] && start < scan[tid] + part) {
+      int acc = scan[tid];
+      for (int j = j0; j < j1; ++j) {
+        const int n = lens.tiles(j);
+        if (start < acc + n) {
+          sm_misc[1] = j;
+          sm_misc[2] = start - acc;
+          break;
+        }
+        acc += n;
+      }
+    }
+    __syncthreads();
+  }
+  const int total = sm_misc[0];
+  const int start = (int)((long long)k * total / P);
+  const int n_items = (int)((long long)(k + 1) * total / P) - start;
+  if (n_items <= 0) return;
+  const int j_start = sm_misc[1], pt_start = sm_misc[2];
+
+  if (tid == kEpiWarps * 32) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiWarps * 32);
+    }
+    mbar_init(bfull, 1);
+    mbar_init(bempty, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kEpiWarps + 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kEpiWarps) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&qmap);
+      ItemIter it;
+      it.init(&lens, j_start, pt_start);
+      int nb = 0, issued = 0, cur_j = -1;
+      bool ok = true;
+      for (int i = 0; i < n_items; ++i, it.next()) {
+        if (it.j != cur_j) {     // new query tile: reload B once the MMA is done with it
+          if (nb > 0) ok = mbar_wait_bounded(bempty, (nb - 1) & 1, kWaitLimitNs);
+          if (!ok || *abort_flag) break;
+          mbar_arrive_expect_tx(bfull, kBBytes);
+          tma_load_2d(sB, &qmap, bfull, 0, it.j * kN);
+          tma_load_2d(sB + kBBytes / 2, &qmap, bfull, 64, it.j * kN);
+          cur_j = it.j;
+          ++nb;
+        }
+        const int s = i % kStages;
+        if (i >= kStages) ok = mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1, kWaitLimitNs);
+        if (!ok || *abort_flag) break;
+        int phys[2];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int page = 2 * it.pt + h;
+          phys[h] = -1;
+          if (page * kPage < it.lmax) {     // a page some query of the tile needs
+            const int ph = __ldg(bt + page);
+            if (ph >= 0 && ph < p.num_pages) {
+              phys[h] = ph;
+              bytes += 2 * kPageHalf;
+            }
+          }
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        uint8_t* st = sA + s * kABytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (phys[h] < 0) continue;
+          tma_load_3d(st + h * kPageHalf, &kmap, &full[s], 0, 0, phys[h]);
+          tma_load_3d(st + kABytes / 2 + h * kPageHalf, &kmap, &full[s], 64, 0, phys[h]);
+        }
+        issued = i + 1;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, DSA_ERR_TIMEOUT);
+      }
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, kWaitLimitNs);
+      if (nb > 0) mbar_wait_bounded(bfull, (nb - 1) & 1, kWaitLimitNs);
+    }
+  } else if (warp == kEpiWarps + 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = instr_desc(1, 1, kTileM, kN);
+      const uint32_t sAa = smem_u32(sA), sBa = smem_u32(sB);
+      ItemIter it;
+      it.init(&lens, j_start, pt_start);
+      int nb = 0, issued = 0, cur_j = -1;
+      bool ok = true;
+      for (int i = 0; i < n_items; ++i) {
+        const int s = i % kStages, a = i & 1;
+        if (it.j != cur_j) {
+          ok = mbar_wait_bounded(bfull, nb & 1, kWaitLimitNs);
+          cur_j = it.j;
+          ++nb;
+        }
+        if (ok) ok = mbar_wait_bounded(&full[s], (i / kStages) & 1, kWaitLimitNs);
+        if (ok && i >= 2) ok = mbar_wait_bounded(&tempty[a], ((i >> 1) - 1) & 1, kWaitLimitNs);
+        if (!ok || *abort_flag) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + a * kN;
+        const uint32_t st = sAa + s * kABytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
+          const uint64_t ad = smem_desc_sw128(st + kb * (kABytes / 2) + ko, 1024);
+          const uint64_t bd = smem_desc_sw128(sBa + kb * (kBBytes / 2) + ko, 1024);
+          mma_f16(d, ad, bd, idesc, kk != 0);
+        }
+        mma_commit(&empty[s]);
+        mma_commit(&tfull[a]);
+        issued = i + 1;
+        it.next();
+        if (i + 1 == n_items || it.j != cur_j) mma_commit(bempty);   // B free after these MMAs
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, DSA_ERR_TIMEOUT);
+      }
+      if (issued > 0) {
+        const int i = issued - 1;
+        mbar_wait_bounded(&tfull[i & 1], (i >> 1) & 1, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps 0-7
+    const int quad = warp & 3;                // TMEM lane quadrant
+    const int qpair = warp >> 2;              // queries 2*qpair, 2*qpair + 1 of the tile
+    const int r = quad * 32 + lane;           // position row inside the tile
+    ItemIter it;
+    it.init(&lens, j_start, pt_start);
+    int cur_j = -1;
+    int Lq[2] = {0, 0};
+    bool badq[2] = {false, false};
+    bool ok = true;
+    for (int i = 0; i < n_items; ++i, it.next()) {
+      const int a = i & 1;
+      if (it.j != cur_j) {
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (tid < kQT * kHeads) {
+          const int qi = kQT * it.j + (tid >> 6);
+          w_s[tid] = qi < p.rows ? __ldg(p.w + (long long)qi * kHeads + (tid & 63)) : 0.f;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        cur_j = it.j;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int qi = kQT * cur_j + 2 * qpair + q;
+          const int L = qi < p.rows ? __ldg(p.seqlens + qi) : 0;
+          badq[q] = L > T;
+          Lq[q] = badq[q] ? 0 : max(L, 0);
+        }
+        // the tail of this query tile past its last position tile
+        if (it.pt == 0) {
+          const int f0 = it.ntl * kTileM;
+          for (int q = 0; q < kQT; ++q) {
+            const int qi = kQT * cur_j + q;
+            if (qi >= p.rows) break;
+            const bool bad = __ldg(p.seqlens + qi) > T;
+            const float fv = bad ? nanf_() : -INFINITY;
+            float* orow = p.out + (long long)qi * p.out_stride;
+            for (int t = f0 + 4 * tid; t < T; t += 4 * kEpiWarps * 32)
+              *reinterpret_cast<float4*>(orow + t) = make_float4(fv, fv, fv, fv);
+            if (bad && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
+          }
+        }
+      }
+      const int t = it.pt * kTileM + r;
+      const int page = t / kPage, slot = t % kPage;
+      const bool in_table = t < T;
+      int phys = -1;
+      float scale = 1.f;
+      if (in_table && (t < Lq[0] || t < Lq[1])) {
+        phys = __ldg(bt + page);
+        if (phys >= 0 && phys < p.num_pages && p.kscale != nullptr)
+          scale = __ldg(reinterpret_cast<const float*>(p.kscale + (long long)phys * p.page_stride) +
+                        slot);
+      }
+      if (ok) ok = mbar_wait_bounded(&tfull[a], (i >> 1) & 1, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);
+      float res[2];
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int qt = 2 * qpair + q;
+          uint32_t v0[32], v1[32];
+          const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + a * kN + qt * kHeads;
+          tmem_ld_32x32b_x32(taddr, v0);
+          tmem_ld_32x32b_x32(taddr + 32, v1);
+          tmem_ld_wait();
+          const float* wq = w_s + qt * kHeads;
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            const float4 wa = *reinterpret_cast<const float4*>(wq + h);
+            const float4 wb = *reinterpret_cast<const float4*>(wq + 32 + h);
+            acc0 = fmaf(wa.x, fmaxf(__uint_as_float(v0[h + 0]), 0.f), acc0);
+            acc1 = fmaf(wb.x, fmaxf(__uint_as_float(v1[h + 0]), 0.f), acc1);
+            acc0 = fmaf(wa.y, fmaxf(__uint_as_float(v0[h + 1]), 0.f), acc0);
+            acc1 = fmaf(wb.y, fmaxf(__uint_as_float(v1[h + 1]), 0.f), acc1);
+            acc0 = fmaf(wa.z, fmaxf(__uint_as_float(v0[h + 2]), 0.f), acc0);
+            acc1 = fmaf(wb.z, fmaxf(__uint_as_float(v1[h + 2]), 0.f), acc1);
+            acc0 = fmaf(wa.w, fmaxf(__uint_as_float(v0[h + 3]), 0.f), acc0);
+            acc1 = fmaf(wb.w, fmaxf(__uint_as_float(v1[h + 3]), 0.f), acc1);
+          }
+          res[q] = acc0 + acc1;
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[a]);
+      }
+      if (in_table) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int qi = kQT * cur_j + 2 * qpair + q;
+          if (qi >= p.rows) continue;
+          float o;
+          if (badq[q]) {
+            o = nanf_();
+          } else if (t >= Lq[q]) {
+            o = -INFINITY;
+          } else if (!ok || phys < 0 || phys >= p.num_pages) {
+            o = nanf_();
+            if (ok) raise_status(p.status, DSA_ERR_BAD_PAGE);
+          } else {
+            o = scale * res[q];
+          }
+          p.out[(long long)qi * p.out_stride + t] = o;
+        }
+      }
+    }
+    if (!ok) raise_status(p.status, DSA_ERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kEpiWarps + 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+  }
+  return n;
+}
+
+cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap kmap, qmap;
+  if (!encode_kcache_map(&kmap, p)) return cudaErrorInvalidValue;
+  if (!encode_q_map(&qmap, p, kN)) return cudaErrorInvalidValue;
+  prefill_kernel<<<sm_count(), kThreads, kSmem, stream>>>(kmap, qmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa
