@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=60.0,
                     help="host-time budget of the reference (oracle) arm")
+    ap.add_argument("--profile", type=int, default=0, metavar="N",
+                    help="only run each call of one step N times (for ncu) and exit")
     return ap.parse_args()
 
 
@@ -250,17 +252,12 @@ def run_ours(args, rank, world, local_rank):
     Wm = max(3, args.warmup if args.warmup is not None else max(3, K // 100))
     S = min(K, 500)                           # steps per captured graph
 
-    def capture(n_steps, offset, timing_events=None):
+    def capture(n_steps, offset):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for i in range(n_steps):
-                cs = copies[(offset + i) % n_copies]
-                for j, c in enumerate(cs):
-                    if timing_events is not None and j == dom_idx:
-                        timing_events[i][0].record()
+                for c in copies[(offset + i) % n_copies]:
                     c()
-                    if timing_events is not None and j == dom_idx:
-                        timing_events[i][1].record()
         return g
 
     # the dominant kernel: the call with the largest algorithmic roofline time
@@ -284,23 +281,11 @@ def run_ours(args, rank, world, local_rank):
         done += min(Wm, S)
     torch.cuda.synchronize()
 
-    # the timed graphs: K = reps * S + rem steps; the dominant call of every
-    # step is bracketed by external timing events inside the graph
-    try:
-        probe = torch.cuda.Event(enable_timing=True, external=True)
-        del probe
-        ext_ok = True
-    except TypeError:
-        ext_ok = False
+    # the timed graphs: K = reps * S + rem steps, no event nodes inside (an
+    # event pair around a launch inside a graph costs microseconds)
     reps, rem = divmod(K, S)
-
-    def ev_pairs(n):
-        return [(torch.cuda.Event(enable_timing=True, external=True),
-                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
-    main_ev = ev_pairs(S) if ext_ok else None
-    rem_ev = ev_pairs(rem) if (ext_ok and rem) else None
-    g_main = capture(S, 0, main_ev)
-    g_rem = capture(rem, (reps * S) % n_copies, rem_ev) if rem else None
+    g_main = capture(S, 0)
+    g_rem = capture(rem, (reps * S) % n_copies) if rem else None
     # one untimed replay of each so that first-replay costs stay outside
     g_main.replay()
     if g_rem is not None:
@@ -317,7 +302,6 @@ def run_ours(args, rank, world, local_rank):
     e1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     e0.record()
-    dom_ms = []
     for _ in range(reps):
         g_main.replay()
     if g_rem is not None:
@@ -329,25 +313,29 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     sampler.stop()
     elapsed_ms = e0.elapsed_time(e1)
-    # per-launch durations of the dominant kernel: the events of the last
-    # replay of each graph hold that replay's timestamps
-    if main_ev is not None:
-        dom_ms += [a.elapsed_time(b) for a, b in main_ev]
-    if rem_ev is not None:
-        dom_ms += [a.elapsed_time(b) for a, b in rem_ev]
-    kernel_timing = "events inside the timed graph (last replay)"
-    if not dom_ms:
-        # torch without external events: time the dominant call alone
-        n = min(S, 200)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n)]
-        for i in range(n):
-            evs[i][0].record()
+
+    # per-launch duration of the dominant kernel: a second timed region of
+    # back-to-back launches of that call alone (rotating copies), events at
+    # the region's ends, on the same stream
+    n_dom = min(2000, max(S, K))
+    g_dom = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_dom):
+        for i in range(min(n_dom, 500)):
             copies[i % n_copies][dom_idx]()
-            evs[i][1].record()
-        torch.cuda.synchronize()
-        dom_ms = [a.elapsed_time(b) for a, b in evs]
-        kernel_timing = "events around eager launches of the dominant call"
+    dom_reps = max(1, n_dom // min(n_dom, 500))
+    g_dom.replay()
+    torch.cuda.synchronize()
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    d0.record()
+    for _ in range(dom_reps):
+        g_dom.replay()
+    d1.record()
+    torch.cuda.synchronize()
+    dom_launches = dom_reps * min(n_dom, 500)
+    dom_ms = [d0.elapsed_time(d1) / dom_launches]
+    kernel_timing = (f"{dom_launches} back-to-back launches of the dominant call "
+                     "(CUDA graph, events at the region's ends)")
 
     # max over ranks
     t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
@@ -400,6 +388,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "gpu_launches": K * len(works),
+        "gpu_launches_kernel_region": dom_launches,
     }
 
     if not args.no_e2e:
@@ -552,9 +541,29 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """Each call of one step, N times in a row, nothing else: the command to
+    put under ncu (launch k of call j is launch k * calls + j)."""
+    import torch
+    from sparse_attention_paged_gb300 import _native
+    _native.load()
+    works = wl.NAMED[args.workload]()
+    calls = [DeviceCall(w, torch.device("cuda", 0)) for w in works]
+    torch.cuda.synchronize()
+    for _ in range(args.profile):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    for c in calls:
+        assert int(c.status.item()) == 0
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

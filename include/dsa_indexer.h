@@ -43,7 +43,10 @@
  *             caller.  The library allocates nothing, never synchronises and
  *             launches exactly one kernel per call on `stream` (a
  *             cudaStream_t; NULL = legacy default stream).  All calls are
- *             legal inside stream capture.
+ *             legal inside stream capture.  The kernel is launched with
+ *             programmatic dependent launch allowed: its set-up may overlap
+ *             the tail of the previous kernel in the stream, but it reads no
+ *             argument array before that kernel has completed.
  *   Shapes.   Only H = 64, D = 128 and page_size = 64 are supported
  *             (DSA_ERR_UNSUPPORTED otherwise).  W >= 1.  Rows may be 0 (no
  *             launch, DSA_OK).
@@ -72,7 +75,10 @@
  *             dev_status is not NULL; the library never clears it (zero it
  *             before the call to read a fresh status).  seqlens[r] <= 0 is
  *             not an error: the row is all -inf.  Entries of the block table
- *             at or past ceil(seqlens[r] / 64) are never read.
+ *             at or past ceil(seqlens[r] / 64) are never used as page ids and
+ *             may hold any value (decode may load the first entries of a row
+ *             before it knows the row's length; all W entries of every row
+ *             must therefore be readable memory).
  */
 #ifndef DSA_INDEXER_H
 #define DSA_INDEXER_H

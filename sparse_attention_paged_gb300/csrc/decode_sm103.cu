@@ -2,7 +2,7 @@
 // GB300 (sm_103a): TMA page gathers through the block table, tcgen05 MMA with
 // the accumulator in TMEM, and a fused ReLU / head-weight / scale epilogue.
 //
-// Grid (G, B), G = min(W, kMaxSlots), fixed by the table width alone, so the
+// Grid (G, B), G = min(W, a per-dtype cap), fixed by the table width alone, so the
 // launch never depends on the lengths and can be captured in a CUDA graph.
 // CTA (c, b) owns the pages c, c+G, c+2G, ... of request b: with G = W this is
 // one CTA per (request, page) ("The Dispatch Wire: Connecting a Triton
@@ -43,16 +43,35 @@ using namespace sm100;
 
 namespace {
 
+#ifndef DSA_DEC_FP8_SLOTS
+#define DSA_DEC_FP8_SLOTS 16
+#endif
+#ifndef DSA_DEC_BF16_SLOTS
+#define DSA_DEC_BF16_SLOTS 32
+#endif
+#ifndef DSA_DEC_FP8_STAGES
+#define DSA_DEC_FP8_STAGES 3
+#endif
+#ifndef DSA_DEC_FP8_CTAS
+#define DSA_DEC_FP8_CTAS 3
+#endif
+#ifndef DSA_DEC_BF16_STAGES
+#define DSA_DEC_BF16_STAGES 2
+#endif
+#ifndef DSA_DEC_BF16_CTAS
+#define DSA_DEC_BF16_CTAS 2
+#endif
 constexpr int kDecThreads = 192;          // warps 0-3 epilogue, 4 TMA, 5 MMA
-constexpr int kMaxSlots = 64;             // G cap: CTAs per request
-constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s bound on any wait
+constexpr long long kWaitLimit = 2000000000ll;   // ~1 s of SM clock: bound on any wait
 
 template <int KV>
 struct DecCfg;
 
 template <>
 struct DecCfg<DSA_KV_FP8_E4M3> {
-  static constexpr int kStages = 5;
+  static constexpr int kStages = DSA_DEC_FP8_STAGES;
+  static constexpr int kCtasPerSm = DSA_DEC_FP8_CTAS;
+  static constexpr int kMaxSlots = DSA_DEC_FP8_SLOTS;     // G cap: CTAs per request
   static constexpr int kPageBytes = kPage * kDim;         // 8 KB of e4m3 rows
   static constexpr int kTileBytes = 2 * kPageBytes;       // 128 rows x 128 B
   static constexpr int kQBytes = 2 * kHeads * kDim;       // hi + lo: 16 KB
@@ -60,14 +79,16 @@ struct DecCfg<DSA_KV_FP8_E4M3> {
 
 template <>
 struct DecCfg<DSA_KV_BF16> {
-  static constexpr int kStages = 2;
+  static constexpr int kStages = DSA_DEC_BF16_STAGES;
+  static constexpr int kCtasPerSm = DSA_DEC_BF16_CTAS;
+  static constexpr int kMaxSlots = DSA_DEC_BF16_SLOTS;
   static constexpr int kPageBytes = kPage * kDim * 2;     // 16 KB
   static constexpr int kTileBytes = 2 * kPageBytes;       // 2 K-blocks x 128 rows x 128 B
   static constexpr int kQBytes = kHeads * kDim * 2;       // 16 KB
 };
 
 // Shared memory: [Q operand][A stages][control: barriers at +0, TMEM slot at
-// +256, abort flag at +260, head weights at +512]; two CTAs fit on an SM.
+// +256, abort flag at +260, head weights at +512]; kCtasPerSm CTAs fit on an SM.
 constexpr int kCtrlBytes = 1024;
 
 template <int KV>
@@ -103,7 +124,7 @@ __device__ __forceinline__ uint32_t to_e4m3x2(float a, float b, float& fa, float
 }  // namespace
 
 template <int KV>
-__global__ void __launch_bounds__(kDecThreads, 2)
+__global__ void __launch_bounds__(kDecThreads, DecCfg<KV>::kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                   const RowsParams p, const int G) {
   using C = DecCfg<KV>;
@@ -128,13 +149,52 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const int warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, b = blockIdx.y;
   const int T = p.W * kPage;
+  float* orow = p.out + (long long)b * p.out_stride;
+  const int* btrow = p.block_table + (long long)b * p.bt_stride;
+
+  // Prologue that reads no input: it may overlap the previous launch.
+  if (tid == 128) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(qbar, KV == DSA_KV_BF16 ? 1 : 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&kmap);
+    if (KV == DSA_KV_BF16) prefetch_tmap(&qmap);
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+
+  // The row length, and (independent of it, so in parallel) the first
+  // tile's block-table entries and, for fp8, the query and head weights.
+  // All of these addresses are inside the caller's arrays whatever the
+  // length; block-table entries past the length are read but never used.
   const int L = __ldg(p.seqlens + b);
+  int bt0 = -1, bt1 = -1;
+  if (tid == 128) {
+    bt0 = __ldg(btrow + c);
+    if (c + G < p.W) bt1 = __ldg(btrow + c + G);
+  }
+  uint2 qraw[16];
+  float wv = 0.f;
+  if (KV == DSA_KV_FP8_E4M3 && warp < 4) {
+    const uint16_t* qrow = p.q + (long long)b * kHeads * kDim;
+#pragma unroll
+    for (int hh = 0; hh < 16; ++hh)
+      qraw[hh] = __ldg(reinterpret_cast<const uint2*>(qrow + (warp * 16 + hh) * kDim) + lane);
+    if (lane < 16) wv = __ldg(p.w + (long long)b * kHeads + warp * 16 + lane);
+  }
+
   const bool bad_len = L > T;
   const int Lc = bad_len ? 0 : max(L, 0);
   const int npv = (Lc + kPage - 1) / kPage;             // valid pages of the row
   const int n_mine = npv > c ? (npv - 1 - c) / G + 1 : 0;
-  float* orow = p.out + (long long)b * p.out_stride;
-  const int* btrow = p.block_table + (long long)b * p.bt_stride;
 
   // -inf (NaN for an over-long row) past the last valid page, split evenly
   // over the row's G CTAs in contiguous 16-byte-aligned chunks.
@@ -156,18 +216,53 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   if (n_mine == 0) return;
   const int n_tiles = (n_mine + 1) >> 1;
 
+  // Producer: page pair i of this CTA -> stage i % S.  pre0/pre1 are
+  // block-table entries already loaded (-2: load here).
+  auto issue_tile = [&](int i, int pre0, int pre1) {
+    const int s = i % S;
+    int phys[2];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int k = 2 * i + h;
+      phys[h] = -1;
+      if (k < n_mine) {
+        const int pre = h == 0 ? pre0 : pre1;
+        const int ph = pre != -2 ? pre : __ldg(btrow + c + k * G);
+        if (ph >= 0 && ph < p.num_pages) {
+          phys[h] = ph;
+          bytes += C::kPageBytes;
+        }
+      }
+    }
+    mbar_arrive_expect_tx(&full[s], bytes);
+    uint8_t* st = sA + s * C::kTileBytes;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (phys[h] < 0) continue;
+      if (KV == DSA_KV_FP8_E4M3) {
+        tma_load_3d(st + h * C::kPageBytes, &kmap, &full[s], 0, 0, phys[h]);
+      } else {
+        // K-block 0 (d 0..63) and K-block 1 (d 64..127), rows of 128 B
+        tma_load_3d(st + h * (C::kPageBytes / 2), &kmap, &full[s], 0, 0, phys[h]);
+        tma_load_3d(st + C::kTileBytes / 2 + h * (C::kPageBytes / 2), &kmap, &full[s], 64, 0,
+                    phys[h]);
+      }
+    }
+  };
+
+  // The first S tiles go out before the setup barrier: this thread
+  // initialised the barriers they signal.
+  int issued = 0;
   if (tid == 128) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    if (KV == DSA_KV_BF16) {
+      mbar_arrive_expect_tx(qbar, C::kQBytes);
+      tma_load_2d(sQ, &qmap, qbar, 0, b * kHeads);
+      tma_load_2d(sQ + C::kQBytes / 2, &qmap, qbar, 64, b * kHeads);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
-    }
-    mbar_init(qbar, KV == DSA_KV_BF16 ? 1 : 128);
-    *abort_flag = 0;
-    fence_barrier_init();
+    const int first = min(S, n_tiles);
+    for (int i = 0; i < first; ++i) issue_tile(i, i == 0 ? bt0 : -2, i == 0 ? bt1 : -2);
+    issued = first;
   }
   if (warp == 5) {
     tmem_alloc(tmem_slot, 128);
@@ -181,55 +276,22 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tmap(&kmap);
-      if (KV == DSA_KV_BF16) {
-        mbar_arrive_expect_tx(qbar, C::kQBytes);
-        tma_load_2d(sQ, &qmap, qbar, 0, b * kHeads);
-        tma_load_2d(sQ + C::kQBytes / 2, &qmap, qbar, 64, b * kHeads);
-      }
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
+      for (int i = issued; i < n_tiles; ++i) {
         const int s = i % S;
-        if (i >= S && !mbar_wait_bounded(&empty[s], ((i / S) - 1) & 1, kWaitLimitNs)) {
+        if (!mbar_wait_bounded(&empty[s], ((i / S) - 1) & 1, kWaitLimit)) {
           *abort_flag = 1;
           raise_status(p.status, DSA_ERR_TIMEOUT);
           break;
         }
         if (*abort_flag) break;
-        int phys[2];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int k = 2 * i + h;
-          phys[h] = -1;
-          if (k < n_mine) {
-            const int ph = __ldg(btrow + c + k * G);
-            if (ph >= 0 && ph < p.num_pages) {
-              phys[h] = ph;
-              bytes += C::kPageBytes;
-            }
-          }
-        }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        uint8_t* st = sA + s * C::kTileBytes;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (phys[h] < 0) continue;
-          if (KV == DSA_KV_FP8_E4M3) {
-            tma_load_3d(st + h * C::kPageBytes / 1, &kmap, &full[s], 0, 0, phys[h]);
-          } else {
-            // K-block 0 (d 0..63) and K-block 1 (d 64..127), rows of 128 B
-            tma_load_3d(st + h * (C::kPageBytes / 2), &kmap, &full[s], 0, 0, phys[h]);
-            tma_load_3d(st + C::kTileBytes / 2 + h * (C::kPageBytes / 2), &kmap, &full[s], 64, 0,
-                        phys[h]);
-          }
-        }
+        issue_tile(i, -2, -2);
         issued = i + 1;
       }
       // never leave the CTA with copies in flight: wait for the last use of
       // every stage (already complete on the normal path)
       for (int i = max(0, issued - S); i < issued; ++i)
-        mbar_wait_bounded(&full[i % S], (i / S) & 1, kWaitLimitNs);
+        mbar_wait_bounded(&full[i % S], (i / S) & 1, kWaitLimit);
+      if (KV == DSA_KV_BF16) mbar_wait_bounded(qbar, 0, kWaitLimit);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -238,12 +300,12 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           KV == DSA_KV_FP8_E4M3 ? instr_desc(0, 0, 128, kHeads) : instr_desc(1, 1, 128, kHeads);
       const uint32_t sQa = smem_u32(sQ);
       const uint32_t sAa = smem_u32(sA);
-      bool ok = mbar_wait_bounded(qbar, 0, kWaitLimitNs);
+      bool ok = mbar_wait_bounded(qbar, 0, kWaitLimit);
       int issued = 0;
       for (int i = 0; ok && i < n_tiles; ++i) {
         const int s = i % S, a = i & 1;
-        ok = mbar_wait_bounded(&full[s], (i / S) & 1, kWaitLimitNs);
-        if (ok && i >= 2) ok = mbar_wait_bounded(&tempty[a], ((i >> 1) - 1) & 1, kWaitLimitNs);
+        ok = mbar_wait_bounded(&full[s], (i / S) & 1, kWaitLimit);
+        if (ok && i >= 2) ok = mbar_wait_bounded(&tempty[a], ((i >> 1) - 1) & 1, kWaitLimit);
         if (!ok || *abort_flag) break;
         tc_fence_after();
         const uint32_t d = tmem_base + a * kHeads;
@@ -280,26 +342,19 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       // the accumulators must be idle before TMEM is released
       if (issued > 0) {
         const int i = issued - 1;
-        mbar_wait_bounded(&tfull[i & 1], (i >> 1) & 1, kWaitLimitNs);
+        mbar_wait_bounded(&tfull[i & 1], (i >> 1) & 1, kWaitLimit);
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue warps 0-3
     if (KV == DSA_KV_FP8_E4M3) {
       // split q[b] into e4m3 hi + lo with a power-of-two scale per head;
-      // warp w owns heads 16w..16w+15, lane l owns d = 4l..4l+3.  All loads
-      // are issued before any use so their latencies overlap.
-      const uint16_t* qrow = p.q + (long long)b * kHeads * kDim;
-      uint2 raw[16];
-#pragma unroll
-      for (int hh = 0; hh < 16; ++hh)
-        raw[hh] = __ldg(reinterpret_cast<const uint2*>(qrow + (warp * 16 + hh) * kDim) + lane);
-      const float wv = lane < 16 ? __ldg(p.w + (long long)b * kHeads + warp * 16 + lane) : 0.f;
+      // warp w owns heads 16w..16w+15, lane l owns d = 4l..4l+3 (loaded above)
 #pragma unroll
       for (int hh = 0; hh < 16; ++hh) {
         const int h = warp * 16 + hh;
-        float x[4] = {bf16f(raw[hh].x & 0xffffu), bf16f(raw[hh].x >> 16),
-                      bf16f(raw[hh].y & 0xffffu), bf16f(raw[hh].y >> 16)};
+        float x[4] = {bf16f(qraw[hh].x & 0xffffu), bf16f(qraw[hh].x >> 16),
+                      bf16f(qraw[hh].y & 0xffffu), bf16f(qraw[hh].y >> 16)};
         float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
         m = warp_max(m);
         int e = 0;
@@ -349,7 +404,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           scale = __ldg(reinterpret_cast<const float*>(p.kscale + (long long)phys * p.page_stride) +
                         slot);
       }
-      if (ok) ok = mbar_wait_bounded(&tfull[a], (i >> 1) & 1, kWaitLimitNs);
+      if (ok) ok = mbar_wait_bounded(&tfull[a], (i >> 1) & 1, kWaitLimit);
       ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);   // warp-uniform for tcgen05.ld
       if (!ok) {
         if (row_valid) orow[t] = t < Lc ? nanf_() : -INFINITY;
@@ -363,19 +418,23 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&tempty[a]);
-      float acc0 = 0.f, acc1 = 0.f;
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 32; h += 4) {
         const float4 wa = *reinterpret_cast<const float4*>(w_s + h);
         const float4 wb = *reinterpret_cast<const float4*>(w_s + 32 + h);
-        acc0 = fmaf(wa.x, fmaxf(__uint_as_float(v0[h + 0]), 0.f), acc0);
-        acc1 = fmaf(wb.x, fmaxf(__uint_as_float(v1[h + 0]), 0.f), acc1);
-        acc0 = fmaf(wa.y, fmaxf(__uint_as_float(v0[h + 1]), 0.f), acc0);
-        acc1 = fmaf(wb.y, fmaxf(__uint_as_float(v1[h + 1]), 0.f), acc1);
-        acc0 = fmaf(wa.z, fmaxf(__uint_as_float(v0[h + 2]), 0.f), acc0);
-        acc1 = fmaf(wb.z, fmaxf(__uint_as_float(v1[h + 2]), 0.f), acc1);
-        acc0 = fmaf(wa.w, fmaxf(__uint_as_float(v0[h + 3]), 0.f), acc0);
-        acc1 = fmaf(wb.w, fmaxf(__uint_as_float(v1[h + 3]), 0.f), acc1);
+        acc0 = __ffma2_rn(make_float2(wa.x, wa.y),
+                          make_float2(fmaxf(__uint_as_float(v0[h]), 0.f),
+                                      fmaxf(__uint_as_float(v0[h + 1]), 0.f)), acc0);
+        acc1 = __ffma2_rn(make_float2(wb.x, wb.y),
+                          make_float2(fmaxf(__uint_as_float(v1[h]), 0.f),
+                                      fmaxf(__uint_as_float(v1[h + 1]), 0.f)), acc1);
+        acc0 = __ffma2_rn(make_float2(wa.z, wa.w),
+                          make_float2(fmaxf(__uint_as_float(v0[h + 2]), 0.f),
+                                      fmaxf(__uint_as_float(v0[h + 3]), 0.f)), acc0);
+        acc1 = __ffma2_rn(make_float2(wb.z, wb.w),
+                          make_float2(fmaxf(__uint_as_float(v1[h + 2]), 0.f),
+                                      fmaxf(__uint_as_float(v1[h + 3]), 0.f)), acc1);
       }
       if (row_valid) {
         float o;
@@ -385,7 +444,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           o = nanf_();
           raise_status(p.status, DSA_ERR_BAD_PAGE);
         } else {
-          o = scale * (acc0 + acc1);
+          o = scale * ((acc0.x + acc0.y) + (acc1.x + acc1.y));
         }
         orow[t] = o;
       }
@@ -404,18 +463,38 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 // ----------------------------------------------------------------------------
 // host side
 
-int decode_slots(int W) { return W < kMaxSlots ? W : kMaxSlots; }
+// CTAs per request, from the launch shape only (never from the lengths, so
+// a captured launch stays valid): at most the per-dtype cap and W; and for a
+// short table (W <= 64 pages, so no request is long) small enough that all
+// B * G CTAs fit in one wave on the GPU.
+template <int KV>
+int decode_slots(int W, int B, int resident_ctas) {
+  int G = W < DecCfg<KV>::kMaxSlots ? W : DecCfg<KV>::kMaxSlots;
+  if (W <= 64 && (long long)B * G > resident_ctas) G = resident_ctas / B;
+  return G < 1 ? 1 : G;
+}
 
 template <int KV>
 static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
-  static bool attr_set = false;
+  // per device: the shared-memory opt-in and the number of resident CTAs
+  static int resident_per_dev[kMaxDevices] = {0};
   constexpr int smem = dec_smem_bytes<KV>();
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<KV>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (resident_per_dev[dev] == 0) {
+    e = cudaFuncSetAttribute(decode_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<KV>,
+                                                           kDecThreads, smem)) != cudaSuccess)
+      return e;
+    resident_per_dev[dev] = sms * (per_sm > 0 ? per_sm : 1);
   }
+  const int resident = resident_per_dev[dev];
   CUtensorMap kmap, qmap;
   if (!encode_kcache_map(&kmap, p)) return cudaErrorInvalidValue;
   if (KV == DSA_KV_BF16) {
@@ -423,10 +502,18 @@ static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
   } else {
     memset(&qmap, 0, sizeof qmap);
   }
-  const int G = decode_slots(p.W);
-  dim3 grid(G, p.rows);
-  decode_kernel<KV><<<grid, kDecThreads, smem, stream>>>(kmap, qmap, p, G);
-  return cudaGetLastError();
+  const int G = decode_slots<KV>(p.W, p.rows, resident);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G, p.rows);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<KV>, kmap, qmap, p, G);
 }
 
 cudaError_t launch_decode(const RowsParams& p, cudaStream_t stream) {

@@ -12,6 +12,7 @@ namespace dsa {
 constexpr int kHeads = 64;      // H
 constexpr int kDim = 128;       // D
 constexpr int kPage = 64;       // positions per page
+constexpr int kMaxDevices = 64; // per-device launch state is kept for this many devices
 
 // Everything a kernel needs about one call (device pointers and sizes).
 struct RowsParams {

@@ -16,9 +16,9 @@
 //
 // Per item: tcgen05 MMA with M = 128 positions, N = 256 (4 queries x 64
 // heads), K = 128, f32 accumulator in TMEM, double-buffered (2 x 256
-// columns); 8 epilogue warps (two per TMEM lane quadrant, one query pair
-// each) apply ReLU, the head weights and the position scale and store one
-// coalesced 128-byte row segment per warp and query.
+// columns); 16 epilogue warps (four per TMEM lane quadrant, one query each)
+// apply ReLU, the head weights (packed f32x2 FMAs) and the position scale and
+// store one coalesced 128-byte row segment per warp.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -37,15 +37,18 @@ namespace {
 constexpr int kQT = 4;                        // queries per tile (N = 256)
 constexpr int kN = kQT * kHeads;              // 256
 constexpr int kTileM = 128;                   // positions per tile
-constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
+#ifndef DSA_PF_STAGES
+#define DSA_PF_STAGES 4
+#endif
+constexpr int kStages = DSA_PF_STAGES;
+constexpr int kEpiWarps = 16;                 // 4 per TMEM lane quadrant, one query each
 constexpr int kThreads = (kEpiWarps + 2) * 32;  // + TMA warp + MMA warp
 constexpr int kABytes = kTileM * kDim * 2;    // 32 KB: 2 K-blocks x 128 rows x 128 B
 constexpr int kBBytes = kN * kDim * 2;        // 64 KB: 2 K-blocks x 256 rows x 128 B
 constexpr int kPageHalf = kPage * 128;        // 8 KB: one page, one K-block
-constexpr int kCtrl = 4096;
+constexpr int kCtrl = 6144;
 constexpr int kSmem = 1024 + kBBytes + kStages * kABytes + kCtrl;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr long long kWaitLimit = 2000000000ll;   // ~1 s of SM clock: bound on any wait
 
 __device__ __forceinline__ float nanf_() { return __int_as_float(0x7fc00000); }
 
@@ -127,6 +130,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Lens lens{T, p.rows, n_qt, p.seqlens};
   const int P = gridDim.x, k = blockIdx.x;
   const int* bt = p.block_table;   // shared row (bt_stride == 0)
+
+  // nothing above reads the call's inputs; from here on they may have been
+  // written by the previous launch in the stream
+  griddep_wait();
+  griddep_launch_dependents();
 
   // ---- fill: rows of query tiles without any position tile (every length
   // <= 0, or over-long rows) are written here; the other tiles' tails are
@@ -220,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int i = 0; i < n_items; ++i, it.next()) {
         if (it.j != cur_j) {     // new query tile: reload B once the MMA is done with it
-          if (nb > 0) ok = mbar_wait_bounded(bempty, (nb - 1) & 1, kWaitLimitNs);
+          if (nb > 0) ok = mbar_wait_bounded(bempty, (nb - 1) & 1, kWaitLimit);
           if (!ok || *abort_flag) break;
           mbar_arrive_expect_tx(bfull, kBBytes);
           tma_load_2d(sB, &qmap, bfull, 0, it.j * kN);
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nb;
         }
         const int s = i % kStages;
-        if (i >= kStages) ok = mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1, kWaitLimitNs);
+        if (i >= kStages) ok = mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit);
         if (!ok || *abort_flag) break;
         int phys[2];
         uint32_t bytes = 0;
@@ -260,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         raise_status(p.status, DSA_ERR_TIMEOUT);
       }
       for (int i = max(0, issued - kStages); i < issued; ++i)
-        mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, kWaitLimitNs);
-      if (nb > 0) mbar_wait_bounded(bfull, (nb - 1) & 1, kWaitLimitNs);
+        mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, kWaitLimit);
+      if (nb > 0) mbar_wait_bounded(bfull, (nb - 1) & 1, kWaitLimit);
     }
   } else if (warp == kEpiWarps + 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -275,12 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_items; ++i) {
         const int s = i % kStages, a = i & 1;
         if (it.j != cur_j) {
-          ok = mbar_wait_bounded(bfull, nb & 1, kWaitLimitNs);
+          ok = mbar_wait_bounded(bfull, nb & 1, kWaitLimit);
           cur_j = it.j;
           ++nb;
         }
-        if (ok) ok = mbar_wait_bounded(&full[s], (i / kStages) & 1, kWaitLimitNs);
-        if (ok && i >= 2) ok = mbar_wait_bounded(&tempty[a], ((i >> 1) - 1) & 1, kWaitLimitNs);
+        if (ok) ok = mbar_wait_bounded(&full[s], (i / kStages) & 1, kWaitLimit);
+        if (ok && i >= 2) ok = mbar_wait_bounded(&tempty[a], ((i >> 1) - 1) & 1, kWaitLimit);
         if (!ok || *abort_flag) break;
         tc_fence_after();
         const uint32_t d = tmem_base + a * kN;
@@ -304,47 +312,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (issued > 0) {
         const int i = issued - 1;
-        mbar_wait_bounded(&tfull[i & 1], (i >> 1) & 1, kWaitLimitNs);
+        mbar_wait_bounded(&tfull[i & 1], (i >> 1) & 1, kWaitLimit);
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue warps 0-7
+    // ------------------------------------------------------------ epilogue warps
     const int quad = warp & 3;                // TMEM lane quadrant
-    const int qpair = warp >> 2;              // queries 2*qpair, 2*qpair + 1 of the tile
+    const int qt = warp >> 2;                 // query of the tile this warp reduces
     const int r = quad * 32 + lane;           // position row inside the tile
+    constexpr int kEpiThreads = kEpiWarps * 32;
     ItemIter it;
     it.init(&lens, j_start, pt_start);
     int cur_j = -1;
-    int Lq[2] = {0, 0};
-    bool badq[2] = {false, false};
+    int Lq = 0, Lmax = 0;
+    bool badq = false;
     bool ok = true;
     for (int i = 0; i < n_items; ++i, it.next()) {
       const int a = i & 1;
       if (it.j != cur_j) {
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         if (tid < kQT * kHeads) {
           const int qi = kQT * it.j + (tid >> 6);
           w_s[tid] = qi < p.rows ? __ldg(p.w + (long long)qi * kHeads + (tid & 63)) : 0.f;
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         cur_j = it.j;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int qi = kQT * cur_j + 2 * qpair + q;
-          const int L = qi < p.rows ? __ldg(p.seqlens + qi) : 0;
-          badq[q] = L > T;
-          Lq[q] = badq[q] ? 0 : max(L, 0);
-        }
+        const int qi = kQT * cur_j + qt;
+        const int L = qi < p.rows ? __ldg(p.seqlens + qi) : 0;
+        badq = L > T;
+        Lq = badq ? 0 : max(L, 0);
+        Lmax = it.lmax;
         // the tail of this query tile past its last position tile
         if (it.pt == 0) {
           const int f0 = it.ntl * kTileM;
           for (int q = 0; q < kQT; ++q) {
-            const int qi = kQT * cur_j + q;
-            if (qi >= p.rows) break;
-            const bool bad = __ldg(p.seqlens + qi) > T;
+            const int qf = kQT * cur_j + q;
+            if (qf >= p.rows) break;
+            const bool bad = __ldg(p.seqlens + qf) > T;
             const float fv = bad ? nanf_() : -INFINITY;
-            float* orow = p.out + (long long)qi * p.out_stride;
-            for (int t = f0 + 4 * tid; t < T; t += 4 * kEpiWarps * 32)
+            float* orow = p.out + (long long)qf * p.out_stride;
+            for (int t = f0 + 4 * tid; t < T; t += 4 * kEpiThreads)
               *reinterpret_cast<float4*>(orow + t) = make_float4(fv, fv, fv, fv);
             if (bad && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
           }
@@ -355,63 +362,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool in_table = t < T;
       int phys = -1;
       float scale = 1.f;
-      if (in_table && (t < Lq[0] || t < Lq[1])) {
+      if (in_table && t < Lmax) {
         phys = __ldg(bt + page);
         if (phys >= 0 && phys < p.num_pages && p.kscale != nullptr)
           scale = __ldg(reinterpret_cast<const float*>(p.kscale + (long long)phys * p.page_stride) +
                         slot);
       }
-      if (ok) ok = mbar_wait_bounded(&tfull[a], (i >> 1) & 1, kWaitLimitNs);
+      if (ok) ok = mbar_wait_bounded(&tfull[a], (i >> 1) & 1, kWaitLimit);
       ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);
-      float res[2];
+      float res = 0.f;
       if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int qt = 2 * qpair + q;
-          uint32_t v0[32], v1[32];
-          const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + a * kN + qt * kHeads;
-          tmem_ld_32x32b_x32(taddr, v0);
-          tmem_ld_32x32b_x32(taddr + 32, v1);
-          tmem_ld_wait();
-          const float* wq = w_s + qt * kHeads;
-          float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-          for (int h = 0; h < 32; h += 4) {
-            const float4 wa = *reinterpret_cast<const float4*>(wq + h);
-            const float4 wb = *reinterpret_cast<const float4*>(wq + 32 + h);
-            acc0 = fmaf(wa.x, fmaxf(__uint_as_float(v0[h + 0]), 0.f), acc0);
-            acc1 = fmaf(wb.x, fmaxf(__uint_as_float(v1[h + 0]), 0.f), acc1);
-            acc0 = fmaf(wa.y, fmaxf(__uint_as_float(v0[h + 1]), 0.f), acc0);
-            acc1 = fmaf(wb.y, fmaxf(__uint_as_float(v1[h + 1]), 0.f), acc1);
-            acc0 = fmaf(wa.z, fmaxf(__uint_as_float(v0[h + 2]), 0.f), acc0);
-            acc1 = fmaf(wb.z, fmaxf(__uint_as_float(v1[h + 2]), 0.f), acc1);
-            acc0 = fmaf(wa.w, fmaxf(__uint_as_float(v0[h + 3]), 0.f), acc0);
-            acc1 = fmaf(wb.w, fmaxf(__uint_as_float(v1[h + 3]), 0.f), acc1);
-          }
-          res[q] = acc0 + acc1;
-        }
+        uint32_t v0[32], v1[32];
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + a * kN + qt * kHeads;
+        tmem_ld_32x32b_x32(taddr, v0);
+        tmem_ld_32x32b_x32(taddr + 32, v1);
+        tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&tempty[a]);
-      }
-      if (in_table) {
+        const float* wq = w_s + qt * kHeads;
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int qi = kQT * cur_j + 2 * qpair + q;
-          if (qi >= p.rows) continue;
-          float o;
-          if (badq[q]) {
-            o = nanf_();
-          } else if (t >= Lq[q]) {
-            o = -INFINITY;
-          } else if (!ok || phys < 0 || phys >= p.num_pages) {
-            o = nanf_();
-            if (ok) raise_status(p.status, DSA_ERR_BAD_PAGE);
-          } else {
-            o = scale * res[q];
-          }
-          p.out[(long long)qi * p.out_stride + t] = o;
+        for (int h = 0; h < 32; h += 4) {
+          const float4 wa = *reinterpret_cast<const float4*>(wq + h);
+          const float4 wb = *reinterpret_cast<const float4*>(wq + 32 + h);
+          acc0 = __ffma2_rn(make_float2(wa.x, wa.y),
+                            make_float2(fmaxf(__uint_as_float(v0[h]), 0.f),
+                                        fmaxf(__uint_as_float(v0[h + 1]), 0.f)), acc0);
+          acc1 = __ffma2_rn(make_float2(wb.x, wb.y),
+                            make_float2(fmaxf(__uint_as_float(v1[h]), 0.f),
+                                        fmaxf(__uint_as_float(v1[h + 1]), 0.f)), acc1);
+          acc0 = __ffma2_rn(make_float2(wa.z, wa.w),
+                            make_float2(fmaxf(__uint_as_float(v0[h + 2]), 0.f),
+                                        fmaxf(__uint_as_float(v0[h + 3]), 0.f)), acc0);
+          acc1 = __ffma2_rn(make_float2(wb.z, wb.w),
+                            make_float2(fmaxf(__uint_as_float(v1[h + 2]), 0.f),
+                                        fmaxf(__uint_as_float(v1[h + 3]), 0.f)), acc1);
         }
+        res = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+      }
+      const int qi = kQT * cur_j + qt;
+      if (in_table && qi < p.rows) {
+        float o;
+        if (badq) {
+          o = nanf_();
+        } else if (t >= Lq) {
+          o = -INFINITY;
+        } else if (!ok || phys < 0 || phys >= p.num_pages) {
+          o = nanf_();
+          if (ok) raise_status(p.status, DSA_ERR_BAD_PAGE);
+        } else {
+          o = scale * res;
+        }
+        p.out[(long long)qi * p.out_stride + t] = o;
       }
     }
     if (!ok) raise_status(p.status, DSA_ERR_TIMEOUT);
@@ -425,30 +428,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 1;
-  }
-  return n;
-}
-
 cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  // per device: the shared-memory opt-in and the SM count (one CTA per SM)
+  static int sms_per_dev[kMaxDevices] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (sms_per_dev[dev] == 0) {
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    sms_per_dev[dev] = sms > 0 ? sms : 1;
   }
   CUtensorMap kmap, qmap;
   if (!encode_kcache_map(&kmap, p)) return cudaErrorInvalidValue;
   if (!encode_q_map(&qmap, p, kN)) return cudaErrorInvalidValue;
-  prefill_kernel<<<sm_count(), kThreads, kSmem, stream>>>(kmap, qmap, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms_per_dev[dev]);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel, kmap, qmap, p);
 }
 
 }  // namespace dsa

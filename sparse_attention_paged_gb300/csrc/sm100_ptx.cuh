@@ -13,10 +13,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
+// ---- programmatic dependent launch ------------------------------------------
+
+// Block until the grids this launch depends on have completed and their
+// memory is visible.  Every thread that reads the call's inputs runs it.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next launch in the stream to start its prologue.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---- mbarrier ---------------------------------------------------------------
@@ -51,16 +58,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`.
-// Returns false on timeout (the caller reports DSA_ERR_TIMEOUT and unwinds).
+// Wait for phase `parity` of `bar` to complete, giving up after about
+// `limit_cycles` SM clock cycles (the SM-local clock is cheap to read; it is
+// sampled every 16 polls).  Returns false on timeout (the caller reports
+// DSA_ERR_TIMEOUT and unwinds).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint64_t limit_ns) {
+                                                  long long limit_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+  const long long t0 = clock64();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0 && clock64() - t0 > limit_cycles) return false;
   }
-  return true;
 }
 
 // ---- TMA ----------------------------------------------------------------------

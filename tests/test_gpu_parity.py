@@ -216,3 +216,55 @@ def test_config5_prefill_full_size_sampled_rows():
 
 def test_prefill_small_full():
     _check_full(wl.prefill_causal("pf_small", 70, 9, 9 * 64 - 75, seed=2))
+
+
+# --- launches overlap their prologue with the previous kernel (programmatic
+# dependent launch): inputs written just before, and outputs written twice
+# back to back, must still be ordered -----------------------------------------
+
+def test_inputs_written_by_the_previous_kernel():
+    import torch
+    w0 = wl.decode_uniform("pdl0", 16, 32, 2048, 512, seed=0)
+    w1 = wl.decode_uniform("pdl1", 16, 32, 2048, 512, seed=1)
+    dw = DeviceWorkload(w0)
+    src = DeviceWorkload(w1)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        # overwrite every input with a device kernel, then call immediately
+        dw.q.copy_(src.q)
+        dw.wt.copy_(src.wt)
+        dw.kcache.copy_(src.kcache)
+        dw.bt.copy_(src.bt)
+        dw.seqlens.copy_(src.seqlens)
+        assert dw.call() == 0
+        out1 = dw.out.clone()
+        dw.q.copy_(DeviceWorkload(w0).q)
+        dw.wt.copy_(DeviceWorkload(w0).wt)
+        dw.kcache.copy_(DeviceWorkload(w0).kcache)
+        dw.bt.copy_(DeviceWorkload(w0).bt)
+        dw.seqlens.copy_(DeviceWorkload(w0).seqlens)
+        assert dw.call() == 0
+    torch.cuda.synchronize()
+    compare(out1.cpu().numpy(), oracle_rows(w1)[0])
+    compare(dw.out.cpu().numpy(), oracle_rows(w0)[0])
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill"])
+def test_back_to_back_calls_into_one_output(kind):
+    """Two calls in a row write the same output buffer; the second's
+    lengths are shorter, so any write of the first landing late would
+    leave a finite value where the second wants -inf."""
+    import torch
+    if kind == "decode":
+        a = wl.decode_with_lengths("bb_a", [2000, 1500, 900, 64], 32, seed=7)
+        b = wl.decode_with_lengths("bb_b", [5, 70, 1, 0], 32, seed=7)
+    else:
+        a = wl.prefill_causal("bb_a", 40, 12, 12 * 64 - 41, seed=8)
+        b = wl.prefill_causal("bb_b", 40, 12, 100, seed=8)
+    da, db = DeviceWorkload(a), DeviceWorkload(b)
+    out = torch.empty_like(da.out)
+    for _ in range(5):
+        assert da.call(out=out) == 0
+        assert db.call(out=out) == 0
+    torch.cuda.synchronize()
+    compare(out.cpu().numpy(), oracle_rows(b)[0])
