@@ -193,6 +193,24 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# aggregation over ranks (weak scaling: every rank runs the same per-GPU work)
+
+def max_over_ranks(elapsed_ms: float, device=None) -> float:
+    """The slowest rank's time: the job is done when every rank is."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, units_per_step: int, elapsed_ms: float) -> float:
+    """Units processed by all ranks per second of the slowest rank's time."""
+    return world * steps * units_per_step / (elapsed_ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # our arm
 
 class DeviceCall:
@@ -337,11 +355,7 @@ def run_ours(args, rank, world, local_rank):
     kernel_timing = (f"{dom_launches} back-to-back launches of the dominant call "
                      "(CUDA graph, events at the region's ends)")
 
-    # max over ranks
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, device)
 
     # status check: the timed calls raised no data error
     for cs in copies:
@@ -349,7 +363,7 @@ def run_ours(args, rank, world, local_rank):
             if int(c.status.item()) != 0:
                 raise RuntimeError(f"kernel status {int(c.status.item())}")
 
-    value = world * K * step_positions / (elapsed_ms / 1e3)
+    value = job_throughput(world, K, step_positions, elapsed_ms)
     dom_avg_s = statistics.mean(dom_ms) / 1e3
     if dom.kind == "prefill":
         achieved = dom.flops() / dom_avg_s / 1e12

@@ -486,6 +486,11 @@ static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
   if (resident_per_dev[dev] == 0) {
     e = cudaFuncSetAttribute(decode_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // all of the unified L1/shared storage as shared memory, so that the
+    // occupancy below (and at run time) is the shared-memory maximum
+    e = cudaFuncSetAttribute(decode_kernel<KV>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
