@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok || *abort_flag) break;
           mbar_arrive_expect_tx(bfull, kBBytes);
           tma_load_2d(sB, &qmap, bfull, 0, it.j * kN);
-          tma_load_2d(sB + kBBytes / 2, &qmap, bfull, 64, it.j * kN);
+          tma_load_2d(sB + kBBytes / 2, &qmap, bfull, kHalfRowUnits, it.j * kN);
           cur_j = it.j;
           ++nb;
         }
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < 2; ++h) {
           if (phys[h] < 0) continue;
           tma_load_3d(st + h * kPageHalf, &kmap, &full[s], 0, 0, phys[h]);
-          tma_load_3d(st + kABytes / 2 + h * kPageHalf, &kmap, &full[s], 64, 0, phys[h]);
+          tma_load_3d(st + kABytes / 2 + h * kPageHalf, &kmap, &full[s], kHalfRowUnits, 0, phys[h]);
         }
         issued = i + 1;
       }

@@ -7,11 +7,16 @@
 
 namespace dsa {
 
-// Key pool: dims {128 values, 64 slots, num_pages}, page stride as given;
-// box = one page (fp8: 128-byte rows; bf16: 64-value halves), 128-byte swizzle.
+// Both maps count in 4-byte units (TMA throughput is per element); a 128-byte
+// row block is 32 units and the second half of a 256-byte bf16 row starts at
+// unit kHalfRowUnits.
+constexpr int kHalfRowUnits = 32;
+
+// Key pool: dims {row bytes / 4, 64 slots, num_pages}, page stride as given;
+// box = one page's 128-byte column block, 128-byte swizzle.
 bool encode_kcache_map(CUtensorMap* m, const RowsParams& p);
 
-// Queries viewed as [rows * 64, 128] bf16; box {64 values, box_rows rows},
+// Queries viewed as [rows * 64, 64 units]; box {32 units, box_rows rows},
 // 128-byte swizzle.
 bool encode_q_map(CUtensorMap* m, const RowsParams& p, int box_rows);
 

@@ -268,3 +268,19 @@ def test_back_to_back_calls_into_one_output(kind):
         assert db.call(out=out) == 0
     torch.cuda.synchronize()
     compare(out.cpu().numpy(), oracle_rows(b)[0])
+
+
+# --- long tables: CTAs are dispatched longest row first -----------------------
+
+@pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
+def test_longest_first_order_with_ties(kv):
+    W = 70
+    lengths = [500, 4000, 500, 4000, 0, W * 64, 1, 4000, -2, 64]
+    _check_full(wl.decode_with_lengths("ties", lengths, W, seed=12, kv_dtype=kv))
+
+
+def test_many_rows_long_table_natural_order():
+    """More rows than the longest-first ordering handles: natural order."""
+    g = np.random.default_rng(13)
+    lengths = g.integers(0, 65 * 64 + 1, 400)
+    _check_full(wl.decode_with_lengths("many", lengths, 65, seed=13))
