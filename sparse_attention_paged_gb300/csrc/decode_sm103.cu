@@ -75,7 +75,10 @@ namespace {
 #endif
 constexpr int kDecThreads = 192;          // warps 0-3 epilogue, 4 TMA, 5 MMA
 constexpr int kCtasPerSm = DSA_DEC_CTAS;
-constexpr long long kWaitLimit = 2000000000ll;   // ~1 s of SM clock: bound on any wait
+#ifndef DSA_WAIT_LIMIT_CYCLES
+#define DSA_WAIT_LIMIT_CYCLES 2000000000ll
+#endif
+constexpr long long kWaitLimit = DSA_WAIT_LIMIT_CYCLES;   // ~1 s of SM clock: bound on any wait
 constexpr int kMaxRowsBalanced = 384;     // balanced mode keeps per-row prefix sums in smem
 
 template <int KV>
@@ -406,6 +409,14 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         const int s = i % S;
         if (i >= S) ok = mbar_wait_bounded(&empty[s], ((i / S) - 1) & 1, kWaitLimit);
         if (!ok || *abort_flag) break;
+#ifdef DSA_TEST_SKIP_FIRST_TILE
+        // test builds only: never deliver the first tile, so that the MMA's
+        // bounded wait for it runs out and the call reports DSA_ERR_TIMEOUT
+        if (i == 0) {
+          issued = i + 1;
+          continue;
+        }
+#endif
         const int* btrow = p.block_table + (long long)it.row * p.bt_stride;
         int phys[2];
         uint32_t bytes = 0;
