@@ -2,6 +2,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <string.h>
+
+#include <mutex>
 
 #include "tensor_maps.cuh"
 
@@ -21,6 +24,68 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// A small cache of encoded maps: a serving loop calls with the same pool
+// and query buffers every step, and encoding is pure host work.  Keyed by
+// everything the encoding reads; direct-mapped, guarded by a mutex.
+struct MapKey {
+  const void* base;
+  unsigned long long dims[3], strides[2];
+  unsigned box[3];
+  int rank;
+  bool operator==(const MapKey& o) const { return memcmp(this, &o, sizeof o) == 0; }
+};
+
+struct MapCacheEntry {
+  bool used;
+  MapKey key;
+  CUtensorMap map;
+};
+
+constexpr int kMapCacheSize = 32;
+MapCacheEntry g_cache[kMapCacheSize];
+std::mutex g_cache_mutex;
+
+int cache_slot(const MapKey& k) {
+  unsigned long long h = reinterpret_cast<unsigned long long>(k.base) >> 4;
+  h ^= k.dims[0] * 0x9E3779B97F4A7C15ull ^ k.dims[1] * 0xC2B2AE3D27D4EB4Full ^ k.dims[2] ^
+       k.strides[1] * 0x165667B19E3779F9ull ^ k.box[1];
+  return (int)(h % kMapCacheSize);
+}
+
+// Encode (or fetch) a 4-byte-unit, 128-byte-swizzle tiled map.
+bool encode_cached(CUtensorMap* m, int rank, const void* base, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box) {
+  MapKey k;
+  memset(&k, 0, sizeof k);
+  k.base = base;
+  k.rank = rank;
+  for (int i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) k.strides[i] = strides[i];
+  const int slot = cache_slot(k);
+  {
+    std::lock_guard<std::mutex> g(g_cache_mutex);
+    if (g_cache[slot].used && g_cache[slot].key == k) {
+      *m = g_cache[slot].map;
+      return true;
+    }
+  }
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, rank, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> g(g_cache_mutex);
+  g_cache[slot].used = true;
+  g_cache[slot].key = k;
+  g_cache[slot].map = *m;
+  return true;
+}
+
 }  // namespace
 
 // TMA moves a bounded number of elements per clock, so every map describes
@@ -32,8 +97,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 128-byte column block (fp8: the whole row; bf16: half a row, the second
 // half at unit coordinate kHalfRowUnits).
 bool encode_kcache_map(CUtensorMap* m, const RowsParams& p) {
-  auto fn = encode_fn();
-  if (!fn) return false;
   const bool bf16 = p.kv_dtype == DSA_KV_BF16;
   const cuuint64_t row_bytes = (cuuint64_t)kDim * (bf16 ? 2 : 1);
   cuuint64_t dims[3] = {row_bytes / 4, (cuuint64_t)kPage, (cuuint64_t)p.num_pages};
@@ -43,27 +106,17 @@ bool encode_kcache_map(CUtensorMap* m, const RowsParams& p) {
 #endif
   const cuuint32_t rows = bf16 ? (cuuint32_t)kPage : (cuuint32_t)DSA_FP8_BOX_ROWS;
   cuuint32_t box[3] = {32u, rows, 1u};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(p.kcache), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_cached(m, 3, p.kcache, dims, strides, box);
 }
 
 // Queries viewed as [rows * 64, 64 units] (a bf16 row of 128 values is 256
 // bytes = 64 units), box {32 units, box_rows}; the second half-row at unit
 // coordinate kHalfRowUnits.
 bool encode_q_map(CUtensorMap* m, const RowsParams& p, int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kDim * 2 / 4, (cuuint64_t)p.rows * kHeads};
   cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
   cuuint32_t box[2] = {32u, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint16_t*>(p.q), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_cached(m, 2, p.q, dims, strides, box);
 }
 
 }  // namespace dsa
