@@ -127,7 +127,10 @@ int dsa_indexer_logits_decode(const void* q, const float* w,
  * Dispatch Decision ...", section "The Problem That Led Here") and length
  * seqlens[i] = its causal limit + 1.  Keys are read page by page from the
  * cache: no gathered copy is made.  kv_dtype DSA_KV_BF16 and bt_stride = 0
- * are supported (DSA_ERR_UNSUPPORTED otherwise).
+ * are supported (DSA_ERR_UNSUPPORTED otherwise).  Range: half of the heads
+ * take their ReLU as a saturating multiply by 2^-64 with the weight scaled
+ * by 2^64, so results are defined for |w[i, h]| < 2^64 and per-head dots
+ * |q . k| < 2^64.
  */
 int dsa_indexer_logits_prefill(const void* q, const float* w,
                                const void* kcache, const void* kscale,

@@ -47,10 +47,20 @@ constexpr int kABytes = kTileM * kDim * 2;    // 32 KB: 2 K-blocks x 128 rows x 
 constexpr int kBBytes = kN * kDim * 2;        // 64 KB: 2 K-blocks x 256 rows x 128 B
 constexpr int kPageHalf = kPage * 128;        // 8 KB: one page, one K-block
 constexpr int kCtrl = 6144;
-constexpr int kSmem = 1024 + kBBytes + kStages * kABytes + kCtrl;
+constexpr int kBtSmem = 4096;                 // block-table entries kept in shared memory
+constexpr int kSmem = 1024 + kBBytes + kStages * kABytes + kCtrl + 4 * kBtSmem;
 constexpr long long kWaitLimit = 2000000000ll;   // ~1 s of SM clock: bound on any wait
 
 __device__ __forceinline__ float nanf_() { return __int_as_float(0x7fc00000); }
+
+// max(s, 0) * 2^-64 for |s| < 2^64, computed on the FMA pipe (a saturating
+// multiply clamps to [0, 1]); the caller's weight carries the 2^64.
+__device__ __forceinline__ float relu_sat(float s) {
+  float r;
+  asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(s), "f"(5.421010862427522e-20f));   // 2^-64
+  return r;
+}
+constexpr float kTwo64 = 18446744073709551616.0f;   // 2^64
 
 struct Lens {
   int T;
@@ -121,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* sm_misc = reinterpret_cast<int*>(ctrl + 272);       // total, start j, start pt
   float* w_s = reinterpret_cast<float*>(ctrl + 1024);      // [4][64]
   int* scan = reinterpret_cast<int*>(ctrl + 2048);         // [kThreads]
+  int* bt_s = reinterpret_cast<int*>(ctrl + kCtrl);        // [kBtSmem] the shared table row
   static_assert((2 * kStages + 6) * 8 <= 256, "control block");
   static_assert(2048 + kThreads * 4 <= kCtrl, "control block");
 
@@ -135,6 +146,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // written by the previous launch in the stream
   griddep_wait();
   griddep_launch_dependents();
+
+  // The one table row all queries share, staged in shared memory (its first
+  // kBtSmem entries): page ids are then read without a global round trip.
+  const int n_bt = min(p.W, kBtSmem);
+  for (int j = tid; j < n_bt; j += kThreads) bt_s[j] = __ldg(bt + j);
+  auto page_id = [&](int page) { return page < kBtSmem ? bt_s[page] : __ldg(bt + page); };
 
   // ---- fill: rows of query tiles without any position tile (every length
   // <= 0, or over-long rows) are written here; the other tiles' tails are
@@ -246,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int page = 2 * it.pt + h;
           phys[h] = -1;
           if (page * kPage < it.lmax) {     // a page some query of the tile needs
-            const int ph = __ldg(bt + page);
+            const int ph = page_id(page);
             if (ph >= 0 && ph < p.num_pages) {
               phys[h] = ph;
               bytes += 2 * kPageHalf;
@@ -333,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         if (tid < kQT * kHeads) {
           const int qi = kQT * it.j + (tid >> 6);
-          w_s[tid] = qi < p.rows ? __ldg(p.w + (long long)qi * kHeads + (tid & 63)) : 0.f;
+          const float wv = qi < p.rows ? __ldg(p.w + (long long)qi * kHeads + (tid & 63)) : 0.f;
+          w_s[tid] = (tid & 2) ? wv * kTwo64 : wv;    // heads 4k+2, 4k+3: see relu_sat
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         cur_j = it.j;
@@ -363,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int phys = -1;
       float scale = 1.f;
       if (in_table && t < Lmax) {
-        phys = __ldg(bt + page);
+        phys = page_id(page);
         if (phys >= 0 && phys < p.num_pages && p.kscale != nullptr)
           scale = __ldg(reinterpret_cast<const float*>(p.kscale + (long long)phys * p.page_stride) +
                         slot);
@@ -381,6 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&tempty[a]);
         const float* wq = w_s + qt * kHeads;
+        // ReLU split over two pipes: heads 4k, 4k+1 by fmax (ALU pipe), heads
+        // 4k+2, 4k+3 by sat(s * 2^-64) (FMA pipe), whose weights are staged
+        // pre-multiplied by 2^64; both are exact for |s| < 2^64.
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < 32; h += 4) {
@@ -393,11 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_float2(fmaxf(__uint_as_float(v1[h]), 0.f),
                                         fmaxf(__uint_as_float(v1[h + 1]), 0.f)), acc1);
           acc0 = __ffma2_rn(make_float2(wa.z, wa.w),
-                            make_float2(fmaxf(__uint_as_float(v0[h + 2]), 0.f),
-                                        fmaxf(__uint_as_float(v0[h + 3]), 0.f)), acc0);
+                            make_float2(relu_sat(__uint_as_float(v0[h + 2])),
+                                        relu_sat(__uint_as_float(v0[h + 3]))), acc0);
           acc1 = __ffma2_rn(make_float2(wb.z, wb.w),
-                            make_float2(fmaxf(__uint_as_float(v1[h + 2]), 0.f),
-                                        fmaxf(__uint_as_float(v1[h + 3]), 0.f)), acc1);
+                            make_float2(relu_sat(__uint_as_float(v1[h + 2])),
+                                        relu_sat(__uint_as_float(v1[h + 3]))), acc1);
         }
         res = (acc0.x + acc0.y) + (acc1.x + acc1.y);
       }
