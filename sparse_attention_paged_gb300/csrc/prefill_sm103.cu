@@ -54,7 +54,7 @@ constexpr long long kWaitLimit = 2000000000ll;   // ~1 s of SM clock: bound on a
 __device__ __forceinline__ float nanf_() { return __int_as_float(0x7fc00000); }
 
 // max(s, 0) * 2^-64 for |s| < 2^64, computed on the FMA pipe (a saturating
-// multiply clamps to [0, 1]); the caller's weight carries the 2^64.
+// multiply clamps to [0, 1]); the caller scales its weighted sum by 2^64.
 __device__ __forceinline__ float relu_sat(float s) {
   float r;
   asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(s), "f"(5.421010862427522e-20f));   // 2^-64
@@ -129,7 +129,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 260);
   int* sm_misc = reinterpret_cast<int*>(ctrl + 272);       // total, start j, start pt
-  float* w_s = reinterpret_cast<float*>(ctrl + 1024);      // [4][64]
   int* scan = reinterpret_cast<int*>(ctrl + 2048);         // [kThreads]
   int* bt_s = reinterpret_cast<int*>(ctrl + kCtrl);        // [kBtSmem] the shared table row
   static_assert((2 * kStages + 6) * 8 <= 256, "control block");
@@ -236,50 +235,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kEpiWarps) {
     // ------------------------------------------------------------ TMA producer
+    // The whole warp walks the item list.  Lane 0 waits on and arms the
+    // barriers; every copy of an item is issued by a lane of its own,
+    // because the copies one thread issues complete one after another while
+    // copies from different threads overlap.
     if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&qmap);
-      ItemIter it;
-      it.init(&lens, j_start, pt_start);
-      int nb = 0, issued = 0, cur_j = -1;
-      bool ok = true;
-      for (int i = 0; i < n_items; ++i, it.next()) {
-        if (it.j != cur_j) {     // new query tile: reload B once the MMA is done with it
+    }
+    ItemIter it;
+    it.init(&lens, j_start, pt_start);
+    int nb = 0, issued = 0, cur_j = -1;
+    bool ok = true;
+    for (int i = 0; i < n_items; ++i, it.next()) {
+      if (it.j != cur_j) {     // new query tile: reload B once the MMA is done with it
+        if (lane == 0) {
           if (nb > 0) ok = mbar_wait_bounded(bempty, (nb - 1) & 1, kWaitLimit);
-          if (!ok || *abort_flag) break;
-          mbar_arrive_expect_tx(bfull, kBBytes);
-          tma_load_2d(sB, &qmap, bfull, 0, it.j * kN);
-          tma_load_2d(sB + kBBytes / 2, &qmap, bfull, kHalfRowUnits, it.j * kN);
-          cur_j = it.j;
-          ++nb;
+          ok = ok && *abort_flag == 0;
+          if (ok) mbar_arrive_expect_tx(bfull, kBBytes);
         }
-        const int s = i % kStages;
-        if (i >= kStages) ok = mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit);
-        if (!ok || *abort_flag) break;
-        int phys[2];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int page = 2 * it.pt + h;
-          phys[h] = -1;
-          if (page * kPage < it.lmax) {     // a page some query of the tile needs
-            const int ph = page_id(page);
-            if (ph >= 0 && ph < p.num_pages) {
-              phys[h] = ph;
-              bytes += 2 * kPageHalf;
-            }
-          }
-        }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        uint8_t* st = sA + s * kABytes;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (phys[h] < 0) continue;
-          tma_load_3d(st + h * kPageHalf, &kmap, &full[s], 0, 0, phys[h]);
-          tma_load_3d(st + kABytes / 2 + h * kPageHalf, &kmap, &full[s], kHalfRowUnits, 0, phys[h]);
-        }
-        issued = i + 1;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane < 2)
+          tma_load_2d(sB + lane * (kBBytes / 2), &qmap, bfull, lane * kHalfRowUnits, it.j * kN);
+        cur_j = it.j;
+        ++nb;
       }
+      const int s = i % kStages;
+      if (lane == 0) {
+        if (i >= kStages) ok = mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit);
+        ok = ok && *abort_flag == 0;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      // lane l < 4: page (l & 1) of the tile, K half (l >> 1)
+      int phys = -1;
+      if (lane < 4) {
+        const int page = 2 * it.pt + (lane & 1);
+        if (page * kPage < it.lmax) {     // a page some query of the tile needs
+          const int ph = page_id(page);
+          if (ph >= 0 && ph < p.num_pages) phys = ph;
+        }
+      }
+      const unsigned have = __ballot_sync(0xffffffffu, phys >= 0);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(have) * kPageHalf);
+      __syncwarp();
+      if (phys >= 0)
+        tma_load_3d(sA + s * kABytes + (lane >> 1) * (kABytes / 2) + (lane & 1) * kPageHalf, &kmap,
+                    &full[s], (lane >> 1) * kHalfRowUnits, 0, phys);
+      issued = i + 1;
+    }
+    if (lane == 0) {
       if (!ok) {
         *abort_flag = 1;
         raise_status(p.status, DSA_ERR_TIMEOUT);
@@ -336,26 +342,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue warps
     const int quad = warp & 3;                // TMEM lane quadrant
     const int qt = warp >> 2;                 // query of the tile this warp reduces
-    const int r = quad * 32 + lane;           // position row inside the tile
+    // Accumulator reads use the 16x256b shape: thread (g = lane / 4,
+    // c = lane % 4) sees rows g, g+8 (first read) and g+16, g+24 (second)
+    // of the quadrant, always at heads 8j + 2c, 8j + 2c + 1 (j < 8), so its
+    // 16 weights stay in registers for a whole query tile.  A reduce-scatter
+    // over the four threads of a row group leaves thread lane with the full
+    // sum of row g + 8 * (2 * (c & 1) + (c >> 1)).
+    const int cq = lane & 3;
+    const int r = quad * 32 + (lane >> 2) + 8 * (2 * (cq & 1) + (cq >> 1));
     constexpr int kEpiThreads = kEpiWarps * 32;
     ItemIter it;
     it.init(&lens, j_start, pt_start);
     int cur_j = -1;
     int Lq = 0, Lmax = 0;
+    float2 wreg[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) wreg[j] = make_float2(0.f, 0.f);
     bool badq = false;
     bool ok = true;
     for (int i = 0; i < n_items; ++i, it.next()) {
       const int a = i & 1;
       if (it.j != cur_j) {
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-        if (tid < kQT * kHeads) {
-          const int qi = kQT * it.j + (tid >> 6);
-          const float wv = qi < p.rows ? __ldg(p.w + (long long)qi * kHeads + (tid & 63)) : 0.f;
-          w_s[tid] = (tid & 2) ? wv * kTwo64 : wv;    // heads 4k+2, 4k+3: see relu_sat
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         cur_j = it.j;
         const int qi = kQT * cur_j + qt;
+        if (qi < p.rows) {
+          const float* wr = p.w + (long long)qi * kHeads + 2 * cq;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) wreg[j] = make_float2(__ldg(wr + 8 * j), __ldg(wr + 8 * j + 1));
+        }
         const int L = qi < p.rows ? __ldg(p.seqlens + qi) : 0;
         badq = L > T;
         Lq = badq ? 0 : max(L, 0);
@@ -391,36 +405,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       float res = 0.f;
       if (ok) {
         tc_fence_after();
-        uint32_t v0[32], v1[32];
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + a * kN + qt * kHeads;
-        tmem_ld_32x32b_x32(taddr, v0);
-        tmem_ld_32x32b_x32(taddr + 32, v1);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&tempty[a]);
-        const float* wq = w_s + qt * kHeads;
-        // ReLU split over two pipes: heads 4k, 4k+1 by fmax (ALU pipe), heads
-        // 4k+2, 4k+3 by sat(s * 2^-64) (FMA pipe), whose weights are staged
-        // pre-multiplied by 2^64; both are exact for |s| < 2^64.
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        float part[4];      // this thread's 16 heads of rows g, g+8, g+16, g+24
 #pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 wa = *reinterpret_cast<const float4*>(wq + h);
-          const float4 wb = *reinterpret_cast<const float4*>(wq + 32 + h);
-          acc0 = __ffma2_rn(make_float2(wa.x, wa.y),
-                            make_float2(fmaxf(__uint_as_float(v0[h]), 0.f),
-                                        fmaxf(__uint_as_float(v0[h + 1]), 0.f)), acc0);
-          acc1 = __ffma2_rn(make_float2(wb.x, wb.y),
-                            make_float2(fmaxf(__uint_as_float(v1[h]), 0.f),
-                                        fmaxf(__uint_as_float(v1[h + 1]), 0.f)), acc1);
-          acc0 = __ffma2_rn(make_float2(wa.z, wa.w),
-                            make_float2(relu_sat(__uint_as_float(v0[h + 2])),
-                                        relu_sat(__uint_as_float(v0[h + 3]))), acc0);
-          acc1 = __ffma2_rn(make_float2(wb.z, wb.w),
-                            make_float2(relu_sat(__uint_as_float(v1[h + 2])),
-                                        relu_sat(__uint_as_float(v1[h + 3]))), acc1);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          tmem_ld_16x256b_x8(taddr + ((uint32_t)(16 * half) << 16), v);
+          tmem_ld_wait();
+          if (half == 1) {
+            tc_fence_before();
+            mbar_arrive(&tempty[a]);
+          }
+          // ReLU split over two pipes: even j by fmax (ALU pipe), odd j by
+          // sat(s * 2^-64) (FMA pipe) in their own sums, scaled back by 2^64.
+          float2 f0 = make_float2(0.f, 0.f), f1 = f0, s0 = f0, s1 = f0;
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            f0 = __ffma2_rn(wreg[j], make_float2(fmaxf(__uint_as_float(v[4 * j]), 0.f),
+                                                 fmaxf(__uint_as_float(v[4 * j + 1]), 0.f)), f0);
+            f1 = __ffma2_rn(wreg[j], make_float2(fmaxf(__uint_as_float(v[4 * j + 2]), 0.f),
+                                                 fmaxf(__uint_as_float(v[4 * j + 3]), 0.f)), f1);
+            s0 = __ffma2_rn(wreg[j + 1], make_float2(relu_sat(__uint_as_float(v[4 * j + 4])),
+                                                     relu_sat(__uint_as_float(v[4 * j + 5]))), s0);
+            s1 = __ffma2_rn(wreg[j + 1], make_float2(relu_sat(__uint_as_float(v[4 * j + 6])),
+                                                     relu_sat(__uint_as_float(v[4 * j + 7]))), s1);
+          }
+          part[2 * half] = (f0.x + f0.y) + kTwo64 * (s0.x + s0.y);
+          part[2 * half + 1] = (f1.x + f1.y) + kTwo64 * (s1.x + s1.y);
         }
-        res = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        // reduce-scatter over c: bit 0 picks rows {g+16, g+24} or {g, g+8},
+        // bit 1 the second or first of the pair
+        const bool b0 = cq & 1, b1 = cq & 2;
+        const float ra = __shfl_xor_sync(0xffffffffu, b0 ? part[0] : part[2], 1);
+        const float rb = __shfl_xor_sync(0xffffffffu, b0 ? part[1] : part[3], 1);
+        const float k0 = (b0 ? part[2] : part[0]) + ra;
+        const float k1 = (b0 ? part[3] : part[1]) + rb;
+        res = (b1 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
       }
       const int qi = kQT * cur_j + qt;
       if (in_table && qi < p.rows) {
