@@ -101,13 +101,20 @@ def read_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources' code: comments and whitespace are left out,
+    so that an edited comment does not disown a profile of the same code."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_paged_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode())
-                h.update(fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                code = fh.read()
+            code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+            code = re.sub(r"//[^\n]*", " ", code)
+            code = re.sub(r"\s+", " ", code)
+            h.update(f.encode())
+            h.update(code.encode())
     return h.hexdigest()[:16]
 
 

@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       const int nthr = n_mine == 0 ? kDecThreads : 128;
       float* orow = p.out + (long long)b * p.out_stride;
       for (long long i = beg + 4 * tid; i < end; i += 4 * nthr)
-        *reinterpret_cast<float4*>(orow + i) = v4;
+        __stcs(reinterpret_cast<float4*>(orow + i), v4);
       if (bad && c == 0 && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
     }
     if (n_mine == 0) return;
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         const long long beg = (long long)(first_page + a) * kPage;
         const long long end = (long long)(first_page + e) * kPage;
         for (long long i = beg + 4 * tid; i < end; i += 4 * nthr)
-          *reinterpret_cast<float4*>(orow + i) = v4;
+          __stcs(reinterpret_cast<float4*>(orow + i), v4);
         if (bad && a == 0 && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
         f = Pf[r] + e;
       }
