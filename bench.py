@@ -49,10 +49,13 @@ WORKLOAD_DESC = {
     "3short_capped": "decode fp8 B=64 W=32 L log-uniform 512..2048",
     "4": "decode bf16 B=64 W=2048 L log-uniform 4096..131072",
     "5": "prefill bf16 n_q=4096 W=352 causal limit 18432+i",
+    "6": "prefill bf16, 4 requests (query tokens, context) = (256, 6144), (512, 12288), "
+         "(128, 3072), (1024, 20480), per-query table rows",
+    "7": "prefill fp8 n_q=1024 W=128 causal limit 7168+i",
 }
 # default (steps, warmup): a timed region of roughly one second per GPU
 DEFAULT_STEPS = {"1": 100000, "2": 100000, "3": 20000, "3ref": 20000, "3short": 40000,
-                 "3short_capped": 100000, "4": 10000, "5": 1000}
+                 "3short_capped": 100000, "4": 10000, "5": 1000, "6": 2000, "7": 5000}
 METRIC = "indexer key-positions scored/s & achieved HBM GB/s (frac of roofline), 1 GB300"
 
 

@@ -99,9 +99,18 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
                           kv_dtype, block_table, bt_stride, seqlens, n_q, H, D,
                           page_size, W, out, out_stride, dev_status, &p);
   if (st != DSA_OK) return st;
-  if (kv_dtype != DSA_KV_BF16 || bt_stride != 0) return DSA_ERR_UNSUPPORTED;
   if (n_q == 0) return DSA_OK;
-  cudaError_t e = dsa::launch_prefill(p, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (kv_dtype == DSA_KV_BF16 && bt_stride == 0) {
+    // one request's queries over one shared table: the query-tile kernel
+    e = dsa::launch_prefill(p, static_cast<cudaStream_t>(stream));
+  } else {
+    // per-query table rows (several requests, multi-token decode) or fp8
+    // keys: every query token is a row of the decode kernel, with its own
+    // table row, length and query
+    if (n_q > 65535) return DSA_ERR_UNSUPPORTED;
+    e = dsa::launch_decode(p, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

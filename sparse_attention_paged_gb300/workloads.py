@@ -77,14 +77,20 @@ class Workload:
         Keys and scales of every valid position, q and w of every row, the
         block-table entries of valid pages, the row lengths, and 4 bytes of
         output for every position of the fixed [R, W*P] output (the -inf fill
-        is part of the contract).  Prefill rows share one block table and one
-        key stream: the keys of the longest row are read once.
+        is part of the contract).  Prefill rows of one request share its
+        block table and key stream: the keys of its longest row are read
+        once.
         """
         per_pos = D + 4 if self.kv_dtype == KV_E4M3 else 2 * D
         L = np.clip(self.seqlens.astype(np.int64), 0, self.W * self.P)
         if self.kind == "prefill" and self.bt_stride == 0:
             key_bytes = int(L.max(initial=0)) * per_pos
             bt_bytes = int(math.ceil(L.max(initial=0) / self.P)) * 4
+        elif self.kind == "prefill" and "groups" in self.meta:
+            # the query tokens of one request share its keys: read once
+            lmax = [int(L[a:a + n].max(initial=0)) for a, n in self.meta["groups"]]
+            key_bytes = sum(lmax) * per_pos
+            bt_bytes = sum(int(math.ceil(m / self.P)) for m in lmax) * 4
         else:
             key_bytes = int(L.sum()) * per_pos
             bt_bytes = int(np.ceil(L / self.P).sum()) * 4
@@ -236,6 +242,35 @@ def prefill_causal(name: str, n_q: int, W: int, first_limit: int, seed: int = 0,
                      meta={"first_limit": first_limit})
 
 
+def prefill_varlen(name: str, requests, seed: int = 0, kv_dtype: int = KV_BF16) -> Workload:
+    """Several requests' prefill chunks in one call: request r brings n_r
+    query tokens at the end of a context of c_r positions (query j of it may
+    see positions 0..c_r - n_r + j), over its own pages of a shuffled pool.
+    Every query token has a block-table row of its own (a copy of its
+    request's row), so bt_stride = W; entries past a request's pages point
+    at one poison page."""
+    g = _gen(seed)
+    reqs = [(int(n), int(c)) for n, c in requests]
+    W = max(int(math.ceil(c / P)) for _, c in reqs)
+    npages = [int(math.ceil(c / P)) for _, c in reqs]
+    n_data = sum(npages)
+    perm = torch.randperm(n_data, generator=g).numpy()
+    poison = n_data
+    rows, lens, groups, off, start = [], [], [], 0, 0
+    for (n, c), k in zip(reqs, npages):
+        row = np.full(W, poison, dtype=np.int64)
+        row[:k] = perm[off:off + k]
+        off += k
+        for j in range(n):
+            rows.append(row)
+            lens.append(c - n + j + 1)
+        groups.append((start, n))
+        start += n
+    bt = np.stack(rows)
+    return _assemble(name, "prefill", kv_dtype, g, W, bt, np.asarray(lens), n_data + 1, W,
+                     meta={"requests": reqs, "groups": groups})
+
+
 # ---------------------------------------------------------------------------
 # The named workloads.
 
@@ -292,6 +327,20 @@ def pages_validation_cases() -> list[Workload]:
     return out
 
 
+def cfg6() -> Workload:
+    """Prefill bf16, four requests in one call with per-query table rows:
+    (query tokens, context) = (256, 6144), (512, 12288), (128, 3072),
+    (1024, 20480)."""
+    return prefill_varlen("prefill_bf16_varlen4_q1920",
+                          [(256, 6144), (512, 12288), (128, 3072), (1024, 20480)], seed=0)
+
+
+def cfg7() -> Workload:
+    """Prefill with fp8 keys: 1,024 query tokens of one request over 128
+    pages (8,192 positions), causal limit of query i = 7168 + i."""
+    return prefill_causal("prefill_fp8_q1024_W128", 1024, 128, 7168, seed=0, kv_dtype=KV_E4M3)
+
+
 NAMED = {
     "1": lambda: [cfg1()],
     "2": lambda: [cfg2a(), cfg2b()],
@@ -301,4 +350,6 @@ NAMED = {
     "3short_capped": lambda: [cfg3_short(32)],
     "4": lambda: [cfg4()],
     "5": lambda: [cfg5()],
+    "6": lambda: [cfg6()],
+    "7": lambda: [cfg7()],
 }

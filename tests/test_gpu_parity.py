@@ -218,6 +218,32 @@ def test_prefill_small_full():
     _check_full(wl.prefill_causal("pf_small", 70, 9, 9 * 64 - 75, seed=2))
 
 
+# --- prefill with per-query table rows (several requests in one call) and
+# with fp8 keys: one decode row per query token ------------------------------
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_E4M3])
+def test_prefill_per_query_tables_small_full(kv):
+    w = wl.prefill_varlen("pf_varlen", [(20, 150), (33, 400), (7, 64), (1, 1)], seed=3, kv_dtype=kv)
+    assert w.bt_stride == w.W
+    _check_full(w)
+
+
+def test_prefill_fp8_shared_table_small_full():
+    _check_full(wl.prefill_causal("pf_fp8", 60, 7, 7 * 64 - 70, seed=4, kv_dtype=wl.KV_E4M3))
+
+
+def test_config6_varlen_prefill_sampled_rows():
+    w = wl.cfg6()
+    rows = []
+    for a, n in w.meta["groups"]:            # first, middle and last token of every request
+        rows += [a, a + n // 2, a + n - 1]
+    _sampled(w, sorted(rows))
+
+
+def test_config7_fp8_prefill_sampled_rows():
+    _sampled(wl.cfg7(), [0, 1, 511, 512, 1022, 1023])
+
+
 # --- launches overlap their prologue with the previous kernel (programmatic
 # dependent launch): inputs written just before, and outputs written twice
 # back to back, must still be ordered -----------------------------------------
