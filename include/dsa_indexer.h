@@ -126,12 +126,13 @@ int dsa_indexer_logits_decode(const void* q, const float* w,
  * (bt_stride = 0: all queries share row 0, the one-request prefill of "The
  * Dispatch Decision ...", section "The Problem That Led Here") and length
  * seqlens[i] = its causal limit + 1.  Keys are read page by page from the
- * cache: no gathered copy is made.  bf16 keys with a shared row (bt_stride =
- * 0) run the query-tile kernel, which reuses each key tile for four query
- * tokens.  Per-query rows (bt_stride >= W: several requests in one call, or
- * multi-token decode) and fp8 keys run the decode kernel with one row per
- * query token; there n_q <= 65535 (DSA_ERR_UNSUPPORTED otherwise).  Range
- * (query-tile kernel): half of the heads
+ * cache: no gathered copy is made.  A shared row (bt_stride = 0) runs the
+ * query-tile kernel, which reuses each key tile for four query tokens (fp8
+ * keys: the query is split into two e4m3 terms, as in decode).  Per-query
+ * rows (bt_stride >= W: several requests in one call, or multi-token
+ * decode) run the decode kernel with one row per query token; there
+ * n_q <= 65535 (DSA_ERR_UNSUPPORTED otherwise).  Range (query-tile kernel,
+ * bf16 keys): half of the heads
  * take their ReLU as a saturating multiply by 2^-64 with the weight scaled
  * by 2^64, so results are defined for |w[i, h]| < 2^64 and per-head dots
  * |q . k| < 2^64.

@@ -101,13 +101,13 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
   if (st != DSA_OK) return st;
   if (n_q == 0) return DSA_OK;
   cudaError_t e;
-  if (kv_dtype == DSA_KV_BF16 && bt_stride == 0) {
+  if (bt_stride == 0) {
     // one request's queries over one shared table: the query-tile kernel
     e = dsa::launch_prefill(p, static_cast<cudaStream_t>(stream));
   } else {
-    // per-query table rows (several requests, multi-token decode) or fp8
-    // keys: every query token is a row of the decode kernel, with its own
-    // table row, length and query
+    // per-query table rows (several requests, multi-token decode): every
+    // query token is a row of the decode kernel, with its own table row,
+    // length and query
     if (n_q > 65535) return DSA_ERR_UNSUPPORTED;
     e = dsa::launch_decode(p, static_cast<cudaStream_t>(stream));
   }

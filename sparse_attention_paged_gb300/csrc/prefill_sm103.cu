@@ -19,7 +19,15 @@
 // columns); 16 epilogue warps (four per TMEM lane quadrant, one query each)
 // apply ReLU, the head weights (packed f32x2 FMAs) and the position scale and
 // store one coalesced 128-byte row segment per warp.
+//
+// Keys in bf16: kind::f16, the query tile loaded by TMA.  Keys in fp8
+// (e4m3): the stored codes are the A operand as they are (kind::f8f6f4, one
+// 8 KB box per page); the query tile is split by the epilogue warps into two
+// e4m3 terms (hi + lo) with a power-of-two scale per head, folded into the
+// head weights, and both terms accumulate into the same TMEM columns.
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <string.h>
@@ -37,19 +45,33 @@ namespace {
 constexpr int kQT = 4;                        // queries per tile (N = 256)
 constexpr int kN = kQT * kHeads;              // 256
 constexpr int kTileM = 128;                   // positions per tile
-#ifndef DSA_PF_STAGES
-#define DSA_PF_STAGES 4
-#endif
-constexpr int kStages = DSA_PF_STAGES;
 constexpr int kEpiWarps = 16;                 // 4 per TMEM lane quadrant, one query each
+constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = (kEpiWarps + 2) * 32;  // + TMA warp + MMA warp
-constexpr int kABytes = kTileM * kDim * 2;    // 32 KB: 2 K-blocks x 128 rows x 128 B
-constexpr int kBBytes = kN * kDim * 2;        // 64 KB: 2 K-blocks x 256 rows x 128 B
-constexpr int kPageHalf = kPage * 128;        // 8 KB: one page, one K-block
+constexpr int kBox = kPage * 128;             // 8 KB: one page's 64 rows of 128 bytes
+constexpr int kBBytes = kN * kDim * 2;        // 64 KB: 2 x 256 rows x 128 B (bf16 K-blocks / e4m3 hi, lo)
 constexpr int kCtrl = 6144;
 constexpr int kBtSmem = 4096;                 // block-table entries kept in shared memory
-constexpr int kSmem = 1024 + kBBytes + kStages * kABytes + kCtrl + 4 * kBtSmem;
 constexpr long long kWaitLimit = 2000000000ll;   // ~1 s of SM clock: bound on any wait
+
+template <int KV>
+struct PfCfg;
+template <>
+struct PfCfg<DSA_KV_BF16> {
+  static constexpr int kStages = 4;
+  static constexpr int kABytes = kTileM * kDim * 2;   // 32 KB: 2 K-blocks x 128 rows x 128 B
+  static constexpr int kOps = 4;                      // boxes per item: page x K-block
+};
+template <>
+struct PfCfg<DSA_KV_FP8_E4M3> {
+  static constexpr int kStages = 8;
+  static constexpr int kABytes = kTileM * kDim;       // 16 KB: 128 rows x 128 B
+  static constexpr int kOps = 2;                      // boxes per item: one per page
+};
+template <int KV>
+constexpr int pf_smem_bytes() {
+  return 1024 + kBBytes + PfCfg<KV>::kStages * PfCfg<KV>::kABytes + kCtrl + 4 * kBtSmem;
+}
 
 __device__ __forceinline__ float nanf_() { return __int_as_float(0x7fc00000); }
 
@@ -61,6 +83,19 @@ __device__ __forceinline__ float relu_sat(float s) {
   return r;
 }
 constexpr float kTwo64 = 18446744073709551616.0f;   // 2^64
+
+// 2^e as a float, e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// Two floats to e4m3 (nearest-even, saturating): the two codes (first
+// argument in the low byte) and their values.
+__device__ __forceinline__ uint32_t to_e4m3x2(float a, float b, float& fa, float& fb) {
+  __nv_fp8x2_storage_t s = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(s, __NV_E4M3);
+  fa = __half2float(__half(__half_raw{h.x}));
+  fb = __half2float(__half(__half_raw{h.y}));
+  return (uint32_t)s;
+}
 
 struct Lens {
   int T;
@@ -111,9 +146,13 @@ struct ItemIter {
 
 }  // namespace
 
+template <int KV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                    const RowsParams p) {
+  constexpr int kStages = PfCfg<KV>::kStages;
+  constexpr int kABytes = PfCfg<KV>::kABytes;
+  constexpr bool kFp8 = KV == DSA_KV_FP8_E4M3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -131,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* sm_misc = reinterpret_cast<int*>(ctrl + 272);       // total, start j, start pt
   int* scan = reinterpret_cast<int*>(ctrl + 2048);         // [kThreads]
   int* bt_s = reinterpret_cast<int*>(ctrl + kCtrl);        // [kBtSmem] the shared table row
+  int* e_s = scan;                                          // fp8: [256] per-head exponents (after the split)
   static_assert((2 * kStages + 6) * 8 <= 256, "control block");
   static_assert(2048 + kThreads * 4 <= kCtrl, "control block");
 
@@ -219,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], kEpiWarps * 32);
     }
-    mbar_init(bfull, 1);
+    mbar_init(bfull, kFp8 ? kEpiThreads : 1);    // fp8: the epilogue threads write B
     mbar_init(bempty, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -240,14 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // little faster than one lane issuing all four).
     if (lane == 0) {
       prefetch_tmap(&kmap);
-      prefetch_tmap(&qmap);
+      if (!kFp8) prefetch_tmap(&qmap);
     }
     ItemIter it;
     it.init(&lens, j_start, pt_start);
     int nb = 0, issued = 0, cur_j = -1;
     bool ok = true;
     for (int i = 0; i < n_items; ++i, it.next()) {
-      if (it.j != cur_j) {     // new query tile: reload B once the MMA is done with it
+      if (!kFp8 && it.j != cur_j) {   // new query tile: reload B once the MMA is done with it
         if (lane == 0) {
           if (nb > 0) ok = mbar_wait_bounded(bempty, (nb - 1) & 1, kWaitLimit);
           ok = ok && *abort_flag == 0;
@@ -267,9 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      // lane l < 4: page (l & 1) of the tile, K half (l >> 1)
+      // lane l < kOps: page (l & 1) of the tile; bf16: K-block (l >> 1)
       int phys = -1;
-      if (lane < 4) {
+      if (lane < PfCfg<KV>::kOps) {
         const int page = 2 * it.pt + (lane & 1);
         if (page * kPage < it.lmax) {     // a page some query of the tile needs
           const int ph = page_id(page);
@@ -277,11 +317,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const unsigned have = __ballot_sync(0xffffffffu, phys >= 0);
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(have) * kPageHalf);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(have) * kBox);
       __syncwarp();
-      if (phys >= 0)
-        tma_load_3d(sA + s * kABytes + (lane >> 1) * (kABytes / 2) + (lane & 1) * kPageHalf, &kmap,
-                    &full[s], (lane >> 1) * kHalfRowUnits, 0, phys);
+      if (phys >= 0) {
+        if (kFp8)
+          tma_load_3d(sA + s * kABytes + lane * kBox, &kmap, &full[s], 0, 0, phys);
+        else
+          tma_load_3d(sA + s * kABytes + (lane >> 1) * (kABytes / 2) + (lane & 1) * kBox, &kmap,
+                      &full[s], (lane >> 1) * kHalfRowUnits, 0, phys);
+      }
       issued = i + 1;
     }
     if (lane == 0) {
@@ -296,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kEpiWarps + 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = instr_desc(1, 1, kTileM, kN);
+      constexpr uint32_t idesc = kFp8 ? instr_desc(0, 0, kTileM, kN) : instr_desc(1, 1, kTileM, kN);
       const uint32_t sAa = smem_u32(sA), sBa = smem_u32(sB);
       ItemIter it;
       it.init(&lens, j_start, pt_start);
@@ -317,10 +361,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = sAa + s * kABytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(st + kb * (kABytes / 2) + ko, 1024);
-          const uint64_t bd = smem_desc_sw128(sBa + kb * (kBBytes / 2) + ko, 1024);
-          mma_f16(d, ad, bd, idesc, kk != 0);
+          if (kFp8) {
+            // hi then lo term; K = 32 per MMA within the 128-byte rows
+            const uint32_t term = kk >> 2, ko = (kk & 3) * 32;
+            const uint64_t ad = smem_desc_sw128(st + ko, 1024);
+            const uint64_t bd = smem_desc_sw128(sBa + term * (kBBytes / 2) + ko, 1024);
+            mma_f8f6f4(d, ad, bd, idesc, kk != 0);
+          } else {
+            const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
+            const uint64_t ad = smem_desc_sw128(st + kb * (kABytes / 2) + ko, 1024);
+            const uint64_t bd = smem_desc_sw128(sBa + kb * (kBBytes / 2) + ko, 1024);
+            mma_f16(d, ad, bd, idesc, kk != 0);
+          }
         }
         mma_commit(&empty[s]);
         mma_commit(&tfull[a]);
@@ -349,7 +401,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     // sum of row g + 8 * (2 * (c & 1) + (c >> 1)).
     const int cq = lane & 3;
     const int r = quad * 32 + (lane >> 2) + 8 * (2 * (cq & 1) + (cq >> 1));
-    constexpr int kEpiThreads = kEpiWarps * 32;
+    // fp8: split query tile j into e4m3 hi + lo terms in B (row q*64 + h,
+    // 128-byte swizzle; hi at +0, lo at +32 KB) with a power-of-two scale
+    // 2^e per head (the head's largest |q| lands in [128, 256)), e in e_s.
+    // Threads 2t and 2t+1 take row t, 64 values each.
+    auto split_queries = [&](int j) {
+      const int row = tid >> 1, half = tid & 1;
+      const int qi = kQT * j + (row >> 6);
+      const bool live = qi < p.rows;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + ((long long)(live ? qi : 0) * kHeads + (row & 63)) * kDim + half * 64);
+      // pass 1: the head's largest |q| (as float bits: non-negative floats
+      // order as integers); pass 2 below re-reads the same 128 bytes (L1)
+      uint32_t mb = 0;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)      // a bf16 pair: low value in bits 0-15
+          mb = max(mb, max((w4[u] << 17) >> 1, (w4[u] >> 16 << 17) >> 1));
+      }
+      float m = __uint_as_float(mb);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      int e = 0;
+      if (m > 0.f) {
+        const int E = ((__float_as_int(m) >> 23) & 0xff) - 127;   // floor(log2 m), m normal
+        e = min(max(7 - E, -126), 126);
+      }
+      const float sc = exp2i(e);
+      if (half == 0) e_s[row] = e;
+      uint8_t* hb = sB + row * 128;
+      uint8_t* lb = sB + kBBytes / 2 + row * 128;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {           // 16 values = one 16-byte chunk of each term
+        const uint4 v0 = live ? __ldg(src + 2 * cc) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 v1 = live ? __ldg(src + 2 * cc + 1) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t src8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float a0 = __uint_as_float(src8[u] << 16) * sc;
+          const float a1 = __uint_as_float(src8[u] & 0xffff0000u) * sc;
+          float h0, h1, l0, l1;
+          const uint32_t hc = to_e4m3x2(a0, a1, h0, h1);
+          const uint32_t lc = to_e4m3x2(a0 - h0, a1 - h1, l0, l1);
+          hi[u >> 1] |= hc << (16 * (u & 1));
+          lo[u >> 1] |= lc << (16 * (u & 1));
+        }
+        const int phys_chunk = (half * 4 + cc) ^ (row & 7);
+        *reinterpret_cast<uint4*>(hb + phys_chunk * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(lb + phys_chunk * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bfull);
+    };
     ItemIter it;
     it.init(&lens, j_start, pt_start);
     int cur_j = -1;
@@ -359,15 +465,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 8; ++j) wreg[j] = make_float2(0.f, 0.f);
     bool badq = false;
     bool ok = true;
+    int nb = 0;           // fp8: query tiles split so far
     for (int i = 0; i < n_items; ++i, it.next()) {
       const int a = i & 1;
       if (it.j != cur_j) {
         cur_j = it.j;
+        if (kFp8) {
+          // every thread is past its reads of the previous e_s; the MMA is
+          // done with the previous B (its last accumulator has been read)
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+          if (nb > 0 && ok) ok = mbar_wait_bounded(bempty, (nb - 1) & 1, kWaitLimit);
+          ++nb;
+          split_queries(cur_j);
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+        }
         const int qi = kQT * cur_j + qt;
         if (qi < p.rows) {
           const float* wr = p.w + (long long)qi * kHeads + 2 * cq;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) wreg[j] = make_float2(__ldg(wr + 8 * j), __ldg(wr + 8 * j + 1));
+          for (int j = 0; j < 8; ++j) {
+            wreg[j] = make_float2(__ldg(wr + 8 * j), __ldg(wr + 8 * j + 1));
+            if (kFp8) {     // undo the split's per-head scale
+              wreg[j].x *= exp2i(-e_s[qt * kHeads + 8 * j + 2 * cq]);
+              wreg[j].y *= exp2i(-e_s[qt * kHeads + 8 * j + 2 * cq + 1]);
+            }
+          }
         }
         const int L = qi < p.rows ? __ldg(p.seqlens + qi) : 0;
         badq = L > T;
@@ -468,17 +590,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream) {
+template <int KV>
+static cudaError_t launch_prefill_t(const RowsParams& p, cudaStream_t stream) {
   // per device: the shared-memory opt-in and the SM count (one CTA per SM)
   static int sms_per_dev[kMaxDevices] = {0};
+  constexpr int smem = pf_smem_bytes<KV>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (sms_per_dev[dev] == 0) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    e = cudaFuncSetAttribute(prefill_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(prefill_kernel<KV>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int sms = 0;
@@ -488,18 +612,27 @@ cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream) {
   }
   CUtensorMap kmap, qmap;
   if (!encode_kcache_map(&kmap, p)) return cudaErrorInvalidValue;
-  if (!encode_q_map(&qmap, p, kN)) return cudaErrorInvalidValue;
+  if (KV == DSA_KV_BF16) {
+    if (!encode_q_map(&qmap, p, kN)) return cudaErrorInvalidValue;
+  } else {
+    memset(&qmap, 0, sizeof qmap);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms_per_dev[dev]);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, kmap, qmap, p);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<KV>, kmap, qmap, p);
+}
+
+cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream) {
+  if (p.kv_dtype == DSA_KV_FP8_E4M3) return launch_prefill_t<DSA_KV_FP8_E4M3>(p, stream);
+  return launch_prefill_t<DSA_KV_BF16>(p, stream);
 }
 
 }  // namespace dsa

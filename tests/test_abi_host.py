@@ -85,9 +85,9 @@ def test_zero_rows_returns_ok_without_launch(lib):
 
 @needs_nvcc
 def test_prefill_mode_checks(lib):
-    # fp8 keys and per-query table rows run one decode row per query token,
-    # whose grid caps n_q at 65535; the checks come before any launch
-    assert call("prefill", kv_dtype=0, bt_stride=0, B=70000) == 2             # fp8 prefill
+    # per-query table rows run one decode row per query token, whose grid
+    # caps n_q at 65535; the checks come before any launch
+    assert call("prefill", kv_dtype=0, bt_stride=8, B=70000) == 2             # fp8, per-query rows
     assert call("prefill", kv_dtype=1, page_stride_bytes=16384, kscale=None,
                 bt_stride=8, B=70000) == 2                                    # per-query tables
     assert call("prefill", kv_dtype=1, page_stride_bytes=16384, kscale=None,

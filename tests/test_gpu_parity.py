@@ -214,8 +214,36 @@ def test_config5_prefill_full_size_sampled_rows():
     _sampled(w, rows)
 
 
-def test_prefill_small_full():
-    _check_full(wl.prefill_causal("pf_small", 70, 9, 9 * 64 - 75, seed=2))
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_E4M3])
+def test_prefill_small_full(kv):
+    # 70 queries: 18 query tiles, the last one ragged
+    _check_full(wl.prefill_causal("pf_small", 70, 9, 9 * 64 - 75, seed=2, kv_dtype=kv))
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_E4M3])
+def test_prefill_bad_page_id(kv):
+    w = wl.prefill_causal("pf_badpage", 30, 6, 6 * 64 - 40, seed=9, kv_dtype=kv)
+    w.block_table = w.block_table.copy()
+    w.block_table[0, 2] = w.num_pages + 3          # positions 128..191, needed by every query
+    dw = _run(w)
+    assert int(dw.status.item()) == 6
+    ref, st = oracle_rows(w)
+    assert st == 6
+    compare(dw.out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_E4M3])
+def test_prefill_length_past_table(kv):
+    w = wl.prefill_causal("pf_badlen", 30, 6, 6 * 64 - 40, seed=10, kv_dtype=kv)
+    w.seqlens = w.seqlens.copy()
+    w.seqlens[5] = w.W * 64 + 1
+    dw = _run(w)
+    assert int(dw.status.item()) == 7
+    ref, st = oracle_rows(w)
+    assert st == 7
+    o = dw.out.cpu().numpy()
+    assert np.isnan(o[5]).all()
+    compare(o, ref)
 
 
 # --- prefill with per-query table rows (several requests in one call) and
@@ -230,6 +258,11 @@ def test_prefill_per_query_tables_small_full(kv):
 
 def test_prefill_fp8_shared_table_small_full():
     _check_full(wl.prefill_causal("pf_fp8", 60, 7, 7 * 64 - 70, seed=4, kv_dtype=wl.KV_E4M3))
+
+
+def test_prefill_fp8_many_query_tiles():
+    # several query tiles per CTA: the query split runs at every tile change
+    _check_full(wl.prefill_causal("pf_fp8_many", 1200, 20, 50, seed=11, kv_dtype=wl.KV_E4M3))
 
 
 def test_config6_varlen_prefill_sampled_rows():
@@ -275,7 +308,7 @@ def test_inputs_written_by_the_previous_kernel():
     compare(dw.out.cpu().numpy(), oracle_rows(w0)[0])
 
 
-@pytest.mark.parametrize("kind", ["decode", "prefill"])
+@pytest.mark.parametrize("kind", ["decode", "prefill", "prefill_fp8"])
 def test_back_to_back_calls_into_one_output(kind):
     """Two calls in a row write the same output buffer; the second's
     lengths are shorter, so any write of the first landing late would
@@ -285,8 +318,9 @@ def test_back_to_back_calls_into_one_output(kind):
         a = wl.decode_with_lengths("bb_a", [2000, 1500, 900, 64], 32, seed=7)
         b = wl.decode_with_lengths("bb_b", [5, 70, 1, 0], 32, seed=7)
     else:
-        a = wl.prefill_causal("bb_a", 40, 12, 12 * 64 - 41, seed=8)
-        b = wl.prefill_causal("bb_b", 40, 12, 100, seed=8)
+        kv = wl.KV_E4M3 if kind == "prefill_fp8" else wl.KV_BF16
+        a = wl.prefill_causal("bb_a", 40, 12, 12 * 64 - 41, seed=8, kv_dtype=kv)
+        b = wl.prefill_causal("bb_b", 40, 12, 100, seed=8, kv_dtype=kv)
     da, db = DeviceWorkload(a), DeviceWorkload(b)
     out = torch.empty_like(da.out)
     for _ in range(5):
