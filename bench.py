@@ -52,10 +52,12 @@ WORKLOAD_DESC = {
     "6": "prefill bf16, 4 requests (query tokens, context) = (256, 6144), (512, 12288), "
          "(128, 3072), (1024, 20480), per-query table rows",
     "7": "prefill fp8 n_q=1024 W=128 causal limit 7168+i",
+    "8": "key-cache store: 65536 bf16 key rows into e4m3 pages (+ scales), random slots of 2048 pages",
 }
 # default (steps, warmup): a timed region of roughly one second per GPU
 DEFAULT_STEPS = {"1": 100000, "2": 100000, "3": 20000, "3ref": 20000, "3short": 40000,
-                 "3short_capped": 100000, "4": 10000, "5": 1000, "6": 2000, "7": 5000}
+                 "3short_capped": 100000, "4": 10000, "5": 1000, "6": 2000, "7": 5000,
+                 "8": 10000}
 METRIC = "indexer key-positions scored/s & achieved HBM GB/s (frac of roofline), 1 GB300"
 
 
@@ -226,9 +228,16 @@ def job_throughput(world: int, steps: int, units_per_step: int, elapsed_ms: floa
 class DeviceCall:
     """One library call with device-resident inputs and its own output."""
 
-    def __init__(self, w: wl.Workload, device):
+    def __init__(self, w, device):
         import torch
         self.w = w
+        self._fn = None
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        if w.kind == "store":
+            self.k = torch.from_numpy(w.k_bits.view(np.int16)).to(device)
+            self.slots = torch.from_numpy(w.slots).to(device)
+            self.kcache = torch.from_numpy(w.kcache).to(device)
+            return
         self.q = torch.from_numpy(w.q_bits.view(np.int16)).to(device)
         self.wt = torch.from_numpy(w.w).to(device)
         self.kcache = torch.from_numpy(w.kcache).to(device)
@@ -238,16 +247,30 @@ class DeviceCall:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.kscale = (None if w.kscale_offset is None
                        else self.kcache.data_ptr() + w.kscale_offset)
-        self._fn = None
 
     def nbytes(self):
-        return sum(t.numel() * t.element_size() for t in
-                   (self.q, self.wt, self.kcache, self.bt, self.seqlens, self.out))
+        if self.w.kind == "store":
+            ts = (self.k, self.slots, self.kcache)
+        else:
+            ts = (self.q, self.wt, self.kcache, self.bt, self.seqlens, self.out)
+        return sum(t.numel() * t.element_size() for t in ts)
+
+    def store(self, k=None, slots=None):
+        import torch
+        import sparse_attention_paged_gb300 as lib
+        w = self.w
+        st = lib.dsa_kcache_store(self.k if k is None else k, self.slots if slots is None else slots,
+                                  w.n, self.kcache, w.page_stride, w.num_pages, w.kv_dtype,
+                                  w.D, w.P, self.status, torch.cuda.current_stream().cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"library call failed: {lib.dsa_status_string(st)}")
 
     def __call__(self, q=None, wt=None, bt=None, seqlens=None, out=None):
         import torch
         import sparse_attention_paged_gb300 as lib
         w = self.w
+        if w.kind == "store":
+            return self.store()
         if self._fn is None:
             self._fn = (lib.dsa_indexer_logits_decode if w.kind == "decode"
                         else lib.dsa_indexer_logits_prefill)
@@ -391,7 +414,7 @@ def run_ours(args, rank, world, local_rank):
         achieved = dom.algorithmic_bytes() / dom_avg_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]}
-    kname = "decode" if dom.kind == "decode" else "prefill"
+    kname = dom.kind
     roof["traffic"] = recorded_traffic(kname, dom.name)
     roof["kernel"] = f"{kname} ({dom.name})"
     roof["algorithmic_bytes_per_launch"] = dom.algorithmic_bytes()
@@ -405,7 +428,9 @@ def run_ours(args, rank, world, local_rank):
         "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 keys x bf16 q -> f32" if dom.kv_dtype == wl.KV_E4M3 else "bf16 -> f32",
+        "dtype": (("bf16 keys -> e4m3 codes + f32 scale" if dom.kv_dtype == wl.KV_E4M3
+                   else "bf16 keys copied") if dom.kind == "store" else
+                  "e4m3 keys x bf16 q -> f32" if dom.kv_dtype == wl.KV_E4M3 else "bf16 -> f32"),
         "data": "synthetic (seeded generator; no dataset)",
         "config": {"workload": WORKLOAD_DESC[args.workload],
                    "calls_per_step": len(works),
@@ -424,7 +449,8 @@ def run_ours(args, rank, world, local_rank):
     }
 
     if not args.no_e2e:
-        line["e2e"] = run_e2e(works, device, min(K, 2000))
+        line["e2e"] = (run_e2e_store(works, device, min(K, 2000)) if dom.kind == "store"
+                       else run_e2e(works, device, min(K, 2000)))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(works)
     if rank == 0:
@@ -490,6 +516,42 @@ def run_e2e(works, device, n_steps):
             "h2d_bytes_per_step": in_total, "d2h_bytes_per_step": out_total}
 
 
+def run_e2e_store(works, device, n_steps):
+    """The store through the public API with host buffers: every step copies
+    its key rows and slots from pinned host memory (one copy per call) and
+    reads the status word back."""
+    import torch
+    calls = [DeviceCall(w, device) for w in works]
+    h_k = [torch.from_numpy(c.w.k_bits.view(np.int16)).pin_memory() for c in calls]
+    h_s = [torch.from_numpy(c.w.slots).pin_memory() for c in calls]
+    d_k = [torch.empty_like(t, device=device) for t in h_k]
+    d_s = [torch.empty_like(t, device=device) for t in h_s]
+    h_st = torch.zeros(len(calls), dtype=torch.int32).pin_memory()
+
+    def step():
+        for j, c in enumerate(calls):
+            d_k[j].copy_(h_k[j], non_blocking=True)
+            d_s[j].copy_(h_s[j], non_blocking=True)
+            c.store(k=d_k[j], slots=d_s[j])
+            h_st[j:j + 1].copy_(c.status, non_blocking=True)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    rows = sum(w.valid_positions for w in works)
+    return {"value": n_steps * rows / (ms / 1e3), "unit": "key-positions/s",
+            "steps": n_steps, "ms_per_step": ms / n_steps,
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_k + h_s),
+            "d2h_bytes_per_step": 4 * len(calls)}
+
+
 # ---------------------------------------------------------------------------
 # the fp64 oracle on the host cores
 
@@ -530,9 +592,31 @@ def _oracle_units(works, units, nthreads):
     return pos
 
 
+def _store_sample(works, budget_s):
+    """The oracle's store on a bounded sample of rows (one thread)."""
+    import oracle
+    w = works[0]
+    cal = min(w.n, 256)
+    pool = w.kcache.copy()
+    t0 = time.perf_counter()
+    oracle.kcache_store(w.k_bits[:cal], w.slots[:cal], pool, w.page_stride, w.num_pages,
+                        w.kv_dtype)
+    t_row = (time.perf_counter() - t0) / cal
+    n = int(min(w.n, max(cal, budget_s / max(t_row, 1e-9))))
+    t0 = time.perf_counter()
+    oracle.kcache_store(w.k_bits[:n], w.slots[:n], pool, w.page_stride, w.num_pages, w.kv_dtype)
+    dt = time.perf_counter() - t0
+    rows = int(((w.slots[:n] >= 0) & (w.slots[:n] < w.num_pages * w.P)).sum())
+    return rows, dt, f"{n} of {w.n} key rows of the workload, {dt:.1f} s, C oracle, one thread"
+
+
 def cpu_baseline(works, budget_s=15.0):
     """The oracle as it stands, on the host cores, on a bounded sample."""
     import oracle
+    if works[0].kind == "store":
+        rows, dt, sample = _store_sample(works, budget_s)
+        return {"value": rows / dt, "unit": "key-positions/s", "cores": 1, "kind": "oracle",
+                "sample": sample}
     cores = oracle.cpu_count()
     total_units = len(_page_sample(works, 10**12))
     # calibrate on a small sample, then size the measured sample to the budget
@@ -558,6 +642,34 @@ def run_reference(args, rank, world):
     works = wl.NAMED[args.workload]()
     K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
     Wm = max(3, args.warmup if args.warmup is not None else 3)
+    if works[0].kind == "store":
+        w = works[0]
+        per_step_budget = args.ref_budget_s / (K + Wm)
+        rows, dt1, _ = _store_sample(works, per_step_budget)
+        n = max(1, min(w.n, int(rows * per_step_budget / max(dt1, 1e-9))))
+        pool = w.kcache.copy()
+        for _ in range(Wm):
+            oracle.kcache_store(w.k_bits[:n], w.slots[:n], pool, w.page_stride, w.num_pages,
+                                w.kv_dtype)
+        t0 = time.perf_counter()
+        for _ in range(K):
+            oracle.kcache_store(w.k_bits[:n], w.slots[:n], pool, w.page_stride, w.num_pages,
+                                w.kv_dtype)
+        dt = time.perf_counter() - t0
+        stored = int(((w.slots[:n] >= 0) & (w.slots[:n] < w.num_pages * w.P)).sum())
+        value = K * stored / dt
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "key-positions/s",
+                "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": dt * 1e3 / K,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32 (the store's decisions)", "data": "synthetic (seeded generator; no dataset)",
+                "config": {"workload": WORKLOAD_DESC[args.workload]},
+                "cpu_baseline": {"value": value, "unit": "key-positions/s", "cores": 1,
+                                 "kind": "oracle",
+                                 "sample": f"each step: {n} of {w.n} key rows, C oracle, one thread"},
+                "e2e": {"value": value, "unit": "key-positions/s",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     cores = oracle.cpu_count()
     total_units = len(_page_sample(works, 10**12))
     cal = _page_sample(works, min(total_units, 2 * cores), seed=1)

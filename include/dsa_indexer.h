@@ -147,6 +147,32 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
                                int* dev_status, void* stream);
 
 /* A static, human-readable name for a status code. */
+/*
+ * Key-cache store: writes n new key rows into their cache slots, in the
+ * page layouts above (the step before the indexer: its keys come from this
+ * cache).  k: bf16 [n, 128], 16-byte aligned.  slot_mapping: int32 [n],
+ * entry i = page * 64 + slot of row i; a negative entry skips the row.
+ * kcache: the pool, page p at (char*)kcache + p * page_stride_bytes.
+ *   DSA_KV_FP8_E4M3  page_stride_bytes >= 8448: the slot's 128 e4m3 codes
+ *                    at page + slot * 128 and its fp32 scale s at
+ *                    page + 8192 + slot * 4, with s = max_d |k[i, d]| / 448
+ *                    (1 for an all-zero row) and code_d = e4m3(k[i, d] / s)
+ *                    rounded to nearest even and saturated to +-448, every
+ *                    step in fp32.  The pages give no quantisation rule; this
+ *                    one maps the row's largest |k| to e4m3's largest finite
+ *                    value, so k ~ code * s.
+ *   DSA_KV_BF16      page_stride_bytes >= 16384: the row's 256 bytes at
+ *                    page + slot * 256.
+ * Host errors as for the indexer calls (D = 128, page_size = 64; k and
+ * kcache 16-byte aligned, page_stride_bytes a multiple of 16).  A slot at or
+ * past num_pages * 64 is skipped and DSA_ERR_BAD_PAGE stored into
+ * *dev_status.  One kernel launch on `stream`; nothing is allocated.  Rows
+ * with the same slot race (the last writer is unspecified).
+ */
+int dsa_kcache_store(const void* k, const int* slot_mapping, int n, void* kcache,
+                     long long page_stride_bytes, int num_pages, int kv_dtype,
+                     int D, int page_size, int* dev_status, void* stream);
+
 const char* dsa_status_string(int status);
 
 /* DSA_INDEXER_ABI_VERSION of the loaded library. */

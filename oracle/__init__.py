@@ -54,7 +54,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
            "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
@@ -77,6 +77,10 @@ def load_library(path: str):
     lib.dsa_oracle_logits.argtypes = [
         vp, vp, vp, vp, ll, ci, ci, vp, ll, vp,
         ci, ci, ci, ci, ci, vp, ll, ci]
+    lib.dsa_oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.dsa_oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.dsa_oracle_kcache_store.restype = ci
+    lib.dsa_oracle_kcache_store.argtypes = [vp, vp, ci, ci, ci, vp, ll, ci, ci]
     return lib
 
 
@@ -138,3 +142,23 @@ def logits(q_bits: np.ndarray, w: np.ndarray, kcache: np.ndarray,
         _ptr(seqlens), int(R), int(H), int(D), int(P), int(W), _ptr(out),
         int(W * P), int(nthreads))
     return out, int(status)
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest e4m3 code to the fp32 value x (ties to even, saturating)."""
+    return int(_load().dsa_oracle_e4m3_encode(float(x)))
+
+
+def kcache_store(k_bits: np.ndarray, slots: np.ndarray, kcache: np.ndarray,
+                 page_stride: int, num_pages: int, kv_dtype: int, D: int = 128,
+                 P: int = 64, lib=None) -> int:
+    """Write the key rows k_bits (bf16 bits [n, D]) into their slots of the
+    byte pool kcache (modified in place); returns the status."""
+    L = lib or _load()
+    k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    sl = np.ascontiguousarray(slots, dtype=np.int32)
+    assert kcache.dtype == np.uint8 and kcache.flags.c_contiguous
+    n = int(sl.shape[0])
+    assert k.shape == (n, D)
+    return int(L.dsa_oracle_kcache_store(_ptr(k), _ptr(sl), n, D, P, _ptr(kcache),
+                                         int(page_stride), int(num_pages), int(kv_dtype)))

@@ -243,3 +243,78 @@ int dsa_oracle_logits(const uint16_t* q, const float* w, const uint8_t* kcache,
   free(tids);
   return status;
 }
+
+/* ---------------------------------------------------------------------------
+ * Key-cache store (the step before the indexer): new key rows k[i] (bf16,
+ * D values) go to slot slot_mapping[i] = page * P + slot of the pool.
+ *
+ * The page layouts are the ones the indexer reads (see the header of this
+ * file).  The pages give no quantisation rule for the fp8 cache; the reading
+ * used here maps a row's largest |k| to e4m3's largest finite value 448:
+ *
+ *   s = max_d |k_d| / 448      (s = 1 when the row is all zero)
+ *   code_d = nearest e4m3 value to k_d / s, ties to the even code,
+ *            magnitudes above 448 saturated to 448
+ *
+ * The scale and the quotients are rounded to fp32, as in the kernel: they
+ * decide integer codes, so both sides take that decision in the same
+ * precision.  The encoder below is the definition itself: it searches the
+ * 127 non-negative finite e4m3 values for the nearest one.
+ * ------------------------------------------------------------------------- */
+
+/* Nearest e4m3 code to x (round to nearest, ties to even mantissa,
+ * saturating to +-448); x is not NaN.  The sign is kept, as in IEEE
+ * rounding: a negative value that rounds to zero gives -0 (0x80). */
+uint8_t dsa_oracle_e4m3_encode(float x) {
+  const double a = fabs((double)x);
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E); /* largest finite: S.1111.110 */
+  int best = 0;
+  double best_d = a; /* distance to code 0 (value 0) */
+  for (int c = 1; c <= 0x7E; ++c) {
+    const double v = dsa_oracle_e4m3_to_double((uint8_t)c);
+    const double d = fabs(a - v);
+    if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+int dsa_oracle_kcache_store(const uint16_t* k, const int32_t* slots, int n, int D, int P,
+                            uint8_t* kcache, long long page_stride, int num_pages,
+                            int kv_dtype) {
+  int status = ORACLE_OK;
+  if (n < 0 || D <= 0 || P <= 0 || num_pages <= 0) return ORACLE_BAD_ARG;
+  for (int i = 0; i < n; ++i) {
+    const int sl = slots[i];
+    if (sl < 0) continue;
+    const int page = sl / P, slot = sl % P;
+    if (page >= num_pages) {
+      status = ORACLE_BAD_PAGE;
+      continue;
+    }
+    uint8_t* pg = kcache + (long long)page * page_stride;
+    const uint16_t* row = k + (long long)i * D;
+    if (kv_dtype == ORACLE_KV_BF16) {
+      memcpy(pg + (long long)slot * D * 2, row, (size_t)D * 2);
+      continue;
+    }
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+      const float v = (float)dsa_oracle_bf16_to_double(row[d]); /* exact */
+      const float av = v < 0.0f ? -v : v;
+      if (av > amax) amax = av;
+    }
+    volatile float s = amax > 0.0f ? amax / 448.0f : 1.0f; /* fp32 division */
+    for (int d = 0; d < D; ++d) {
+      const float v = (float)dsa_oracle_bf16_to_double(row[d]);
+      volatile float x = v / s; /* fp32 division */
+      pg[(long long)slot * D + d] = dsa_oracle_e4m3_encode(x);
+    }
+    float sv = s;
+    memcpy(pg + (long long)P * D + (long long)slot * 4, &sv, 4);
+  }
+  return status;
+}

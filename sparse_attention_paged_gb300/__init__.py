@@ -85,6 +85,14 @@ def dsa_indexer_logits_prefill(q, w, kcache, kscale, page_stride_bytes, num_page
         _stream(stream)))
 
 
+def dsa_kcache_store(k, slot_mapping, n, kcache, page_stride_bytes, num_pages, kv_dtype,
+                     D, page_size, dev_status=None, stream=None) -> int:
+    """C ``dsa_kcache_store``; returns its status code."""
+    return int(_native.load().dsa_kcache_store(
+        _p(k), _p(slot_mapping), int(n), _p(kcache), int(page_stride_bytes), int(num_pages),
+        int(kv_dtype), int(D), int(page_size), _p(dev_status), _stream(stream)))
+
+
 def indexer_logits(kind: str, q, w, kcache, kscale, page_stride_bytes, num_pages,
                    kv_dtype, block_table, bt_stride, seqlens, W, out=None,
                    dev_status=None, stream=None):

@@ -9,6 +9,9 @@
 namespace dsa {
 cudaError_t launch_decode(const RowsParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream);
+cudaError_t launch_store(const uint16_t* k, const int* slots, int n, uint8_t* kcache,
+                         long long page_stride, int num_pages, int kv_dtype, int* status,
+                         cudaStream_t stream);
 }
 
 namespace {
@@ -111,6 +114,28 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
     if (n_q > 65535) return DSA_ERR_UNSUPPORTED;
     e = dsa::launch_decode(p, static_cast<cudaStream_t>(stream));
   }
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_kcache_store(const void* k, const int* slot_mapping, int n, void* kcache,
+                     long long page_stride_bytes, int num_pages, int kv_dtype, int D,
+                     int page_size, int* dev_status, void* stream) {
+  if (D != dsa::kDim || page_size != dsa::kPage) return DSA_ERR_UNSUPPORTED;
+  if (kv_dtype != DSA_KV_FP8_E4M3 && kv_dtype != DSA_KV_BF16) return DSA_ERR_INVALID_ARG;
+  if (n < 0 || num_pages <= 0) return DSA_ERR_INVALID_ARG;
+  if (n > 0 && (!k || !slot_mapping || !kcache)) return DSA_ERR_INVALID_ARG;
+  // fp8: codes then scales in one page; bf16: the values
+  const long long need = kv_dtype == DSA_KV_FP8_E4M3
+                             ? (long long)dsa::kPage * (dsa::kDim + 4)
+                             : (long long)dsa::kPage * dsa::kDim * 2;
+  if (page_stride_bytes < need) return DSA_ERR_INVALID_ARG;
+  if (page_stride_bytes % 16 != 0 || !aligned(k, 16) || !aligned(kcache, 16) ||
+      !aligned(slot_mapping, 4))
+    return DSA_ERR_MISALIGNED;
+  if (n == 0) return DSA_OK;
+  cudaError_t e = dsa::launch_store(static_cast<const uint16_t*>(k), slot_mapping, n,
+                                    static_cast<uint8_t*>(kcache), page_stride_bytes, num_pages,
+                                    kv_dtype, dev_status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

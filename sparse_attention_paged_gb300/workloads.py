@@ -327,6 +327,65 @@ def pages_validation_cases() -> list[Workload]:
     return out
 
 
+@dataclass
+class StoreWorkload:
+    """One key-cache store call: n new key rows and their slots, plus the
+    pool they go into (host-resident; unwritten slots keep their poison)."""
+    name: str
+    kv_dtype: int
+    k_bits: np.ndarray          # uint16 [n, D], bf16 bit patterns
+    slots: np.ndarray           # int32 [n]: page * P + slot, < 0 = skip
+    kcache: np.ndarray          # uint8 [num_pages * page_stride]
+    page_stride: int
+    num_pages: int
+    kind: str = "store"
+    D: int = D
+    P: int = P
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def n(self) -> int:
+        return int(self.slots.shape[0])
+
+    @property
+    def valid_positions(self) -> int:
+        """Rows actually stored (the store's unit of work)."""
+        return int(((self.slots >= 0) & (self.slots < self.num_pages * self.P)).sum())
+
+    def algorithmic_bytes(self) -> int:
+        """Every row's 256 bytes of bf16 and 4-byte slot are read; each stored
+        row writes D codes + a 4-byte scale (fp8) or 2*D bytes (bf16)."""
+        written = (self.D + 4) if self.kv_dtype == KV_E4M3 else 2 * self.D
+        return self.n * (2 * self.D + 4) + self.valid_positions * written
+
+    def flops(self) -> int:
+        return 0
+
+
+def store_rows(name: str, n: int, num_pages: int, seed: int = 0, kv_dtype: int = KV_E4M3,
+               n_skip: int = 0, n_bad: int = 0) -> StoreWorkload:
+    """n key rows of N(0, 1) x a per-row factor U[0.01, 50] (bf16), stored to
+    distinct random slots of a pool of num_pages pages; n_skip of them carry
+    slot -1 and n_bad a slot past the pool."""
+    g = _gen(seed)
+    x = torch.randn(n, D, generator=g) * (torch.rand(n, 1, generator=g) * 49.99 + 0.01)
+    k = _bf16_bits(x).reshape(n, D)
+    slots = torch.randperm(num_pages * P, generator=g)[:n].numpy().astype(np.int32)
+    pick = torch.randperm(n, generator=g).numpy()
+    slots[pick[:n_skip]] = -1
+    slots[pick[n_skip:n_skip + n_bad]] = num_pages * P + pick[n_skip:n_skip + n_bad]
+    stride = FP8_PAGE_BYTES if kv_dtype == KV_E4M3 else BF16_PAGE_BYTES
+    pool = np.full(num_pages * stride, 0xA5, dtype=np.uint8)
+    return StoreWorkload(name=name, kv_dtype=kv_dtype, k_bits=k, slots=slots, kcache=pool,
+                         page_stride=stride, num_pages=num_pages)
+
+
+def cfg8() -> StoreWorkload:
+    """Key-cache store, bf16 rows to fp8 pages: 65,536 rows (a long prefill
+    chunk) into random slots of a 2,048-page pool."""
+    return store_rows("store_fp8_n65536", 65536, 2048, seed=0)
+
+
 def cfg6() -> Workload:
     """Prefill bf16, four requests in one call with per-query table rows:
     (query tokens, context) = (256, 6144), (512, 12288), (128, 3072),
@@ -352,4 +411,5 @@ NAMED = {
     "5": lambda: [cfg5()],
     "6": lambda: [cfg6()],
     "7": lambda: [cfg7()],
+    "8": lambda: [cfg8()],
 }

@@ -92,3 +92,30 @@ def test_prefill_mode_checks(lib):
                 bt_stride=8, B=70000) == 2                                    # per-query tables
     assert call("prefill", kv_dtype=1, page_stride_bytes=16384, kscale=None,
                 bt_stride=0, B=0) == 0
+
+
+def store_call(**kw):
+    import sparse_attention_paged_gb300 as s
+    args = dict(k=A, slot_mapping=A, n=4, kcache=A, page_stride_bytes=8448, num_pages=16,
+                kv_dtype=0, D=128, page_size=64, dev_status=None, stream=0)
+    args.update(kw)
+    return s.dsa_kcache_store(**args)
+
+
+@needs_nvcc
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=64), 2), (dict(page_size=32), 2), (dict(kv_dtype=3), 1), (dict(n=-1), 1),
+    (dict(num_pages=0), 1), (dict(k=None), 1), (dict(kcache=None), 1),
+    (dict(slot_mapping=None), 1),
+    (dict(page_stride_bytes=8192), 1),                    # fp8 pages need room for the scales
+    (dict(kv_dtype=1, page_stride_bytes=8448), 1),        # bf16 pages hold 16 KB of values
+    (dict(page_stride_bytes=8456), 3), (dict(k=A + 8), 3), (dict(kcache=A + 4), 3),
+    (dict(slot_mapping=A + 2), 3),
+])
+def test_store_rejects_bad_arguments(lib, kw, code):
+    assert store_call(**kw) == code
+
+
+@needs_nvcc
+def test_store_zero_rows_is_a_no_op(lib):
+    assert store_call(n=0) == 0
