@@ -105,14 +105,23 @@ def read_peaks():
             "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS_SUSTAINED, "source": "fallback"}
 
 
-def kernel_source_hash():
-    """Hash of the kernel sources' code: comments and whitespace are left out,
-    so that an edited comment does not disown a profile of the same code."""
+KERNEL_SOURCES = {   # each kernel's own source and the shared code it includes
+    kind: (f"{kind}_sm103.cu", "dsa_common.cuh", "sm100_ptx.cuh", "tensor_maps.cu",
+           "tensor_maps.cuh")
+    for kind in ("decode", "prefill", "store")
+}
+
+
+def kernel_source_hash(kernel: str | None = None):
+    """Hash of a kernel's source code (all kernels' when kernel is None):
+    comments and whitespace are left out, so that an edited comment does not
+    disown a profile of the same code."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_paged_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
+    names = KERNEL_SOURCES[kernel] if kernel else os.listdir(csrc)
+    for f in sorted(names):
+        if f.endswith((".cu", ".cuh")) and os.path.exists(os.path.join(csrc, f)):
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 code = fh.read()
             code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
@@ -131,7 +140,7 @@ def recorded_traffic(kernel: str, workload: str):
         with open(path) as f:
             d = json.load(f)
         e = d.get(f"{kernel}@{workload}")
-        if e and e.get("kernel_source_hash") == kernel_source_hash():
+        if e and e.get("kernel_source_hash") == kernel_source_hash(kernel):
             return float(e["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         pass
