@@ -53,11 +53,12 @@ WORKLOAD_DESC = {
          "(128, 3072), (1024, 20480), per-query table rows",
     "7": "prefill fp8 n_q=1024 W=128 causal limit 7168+i",
     "8": "key-cache store: 65536 bf16 key rows into e4m3 pages (+ scales), random slots of 2048 pages",
+    "9": "decode fp8 B=64 W=4097 L log-uniform 512..32768, top-2048 positions per request",
 }
 # default (steps, warmup): a timed region of roughly one second per GPU
 DEFAULT_STEPS = {"1": 100000, "2": 100000, "3": 20000, "3ref": 20000, "3short": 40000,
                  "3short_capped": 100000, "4": 10000, "5": 1000, "6": 2000, "7": 5000,
-                 "8": 10000}
+                 "8": 10000, "9": 20000}
 METRIC = "indexer key-positions scored/s & achieved HBM GB/s (frac of roofline), 1 GB300"
 
 
@@ -110,6 +111,7 @@ KERNEL_SOURCES = {   # each kernel's own source and the shared code it includes
            "tensor_maps.cuh")
     for kind in ("decode", "prefill", "store")
 }
+KERNEL_SOURCES["topk"] = KERNEL_SOURCES["decode"] + ("topk_sm103.cu",)   # decode, then selection
 
 
 def kernel_source_hash(kernel: str | None = None):
@@ -252,7 +254,14 @@ class DeviceCall:
         self.kcache = torch.from_numpy(w.kcache).to(device)
         self.bt = torch.from_numpy(w.block_table).to(device)
         self.seqlens = torch.from_numpy(w.seqlens).to(device)
-        self.out = torch.empty((w.R, w.W * w.P), dtype=torch.float32, device=device)
+        if w.kind == "topk":
+            k = w.meta["k_top"]
+            self.idx = torch.empty((w.R, k), dtype=torch.int32, device=device)
+            self.val = torch.empty((w.R, k), dtype=torch.float32, device=device)
+            self.ws = torch.empty(w.R * w.W * w.P, dtype=torch.float32, device=device)
+            self.out = self.idx
+        else:
+            self.out = torch.empty((w.R, w.W * w.P), dtype=torch.float32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.kscale = (None if w.kscale_offset is None
                        else self.kcache.data_ptr() + w.kscale_offset)
@@ -260,6 +269,8 @@ class DeviceCall:
     def nbytes(self):
         if self.w.kind == "store":
             ts = (self.k, self.slots, self.kcache)
+        elif self.w.kind == "topk":
+            ts = (self.q, self.wt, self.kcache, self.bt, self.seqlens, self.idx, self.val, self.ws)
         else:
             ts = (self.q, self.wt, self.kcache, self.bt, self.seqlens, self.out)
         return sum(t.numel() * t.element_size() for t in ts)
@@ -280,6 +291,21 @@ class DeviceCall:
         w = self.w
         if w.kind == "store":
             return self.store()
+        if w.kind == "topk":
+            k = w.meta["k_top"]
+            st = lib.dsa_indexer_topk_decode(
+                self.q if q is None else q, self.wt if wt is None else wt, self.kcache,
+                self.kscale, w.page_stride, w.num_pages, w.kv_dtype,
+                self.bt if bt is None else bt, w.bt_stride,
+                self.seqlens if seqlens is None else seqlens, w.R, w.H, w.D, w.P, w.W, k,
+                self.idx, self.val, k, self.ws, self.ws.numel(), self.status,
+                torch.cuda.current_stream().cuda_stream)
+            if st != 0:
+                raise RuntimeError(f"library call failed: {lib.dsa_status_string(st)}")
+            if out is not None and out is not self.idx:     # e2e: both results to one buffer
+                out[:, :k].copy_(self.idx.view(torch.float32))
+                out[:, k:].copy_(self.val)
+            return
         if self._fn is None:
             self._fn = (lib.dsa_indexer_logits_decode if w.kind == "decode"
                         else lib.dsa_indexer_logits_prefill)
@@ -495,7 +521,8 @@ def run_e2e(works, device, n_steps):
         n = t.numel() * t.element_size()
         h_in[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
         views.append(d_in[o:o + n].view(t.dtype).view(t.shape))
-    outs_meta = [torch.empty(c.out.shape, dtype=torch.float32) for c in calls]
+    outs_meta = [torch.empty((c.w.R, 2 * c.w.meta["k_top"]) if c.w.kind == "topk" else c.out.shape,
+                             dtype=torch.float32) for c in calls]
     out_offs, out_total = pack(outs_meta)
     d_out = torch.empty(out_total, dtype=torch.uint8, device=device)
     h_out = torch.empty(out_total, dtype=torch.uint8).pin_memory()

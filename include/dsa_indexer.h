@@ -148,6 +148,31 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
 
 /* A static, human-readable name for a status code. */
 /*
+ * Decode with top-k selection: for every request b, the k_top positions
+ * t < seqlens[b] with the largest logits (the positions sparse attention
+ * then reads), instead of the [B, W*64] logits.  topk_idx: int32, row b at
+ * topk_idx + b * topk_stride (topk_stride >= k_top), the selected positions
+ * in increasing order; a row with L <= k_top valid positions takes all of
+ * them and pads with -1.  topk_val (nullable): their logits, same layout,
+ * -inf for the padding.  Equal logits at the k-th place are taken in
+ * position order.  workspace: device fp32 buffer of at least
+ * B * W * 64 entries (16-byte aligned) that receives the logits of the valid
+ * positions only (no -inf fill, so the output bytes of a long table are not
+ * written); the caller owns it.  Two kernel launches on `stream`: the
+ * decode kernel, then the selection (one CTA per request, a three-pass
+ * radix select).  Other arguments, checks and data errors as for
+ * dsa_indexer_logits_decode; an over-long row selects nothing (all -1) and
+ * reports DSA_ERR_BAD_SEQLEN.
+ */
+int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
+                            const void* kscale, long long page_stride_bytes, int num_pages,
+                            int kv_dtype, const int* block_table, long long bt_stride,
+                            const int* seqlens, int B, int H, int D, int page_size, int W,
+                            int k_top, int* topk_idx, float* topk_val, long long topk_stride,
+                            float* workspace, long long workspace_floats, int* dev_status,
+                            void* stream);
+
+/*
  * Key-cache store: writes n new key rows into their cache slots, in the
  * page layouts above (the step before the indexer: its keys come from this
  * cache).  k: bf16 [n, 128], 16-byte aligned.  slot_mapping: int32 [n],

@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       int chunk = (T - f0 + G - 1) / G;
       chunk = (chunk + 3) & ~3;
       const long long beg = f0 + (long long)c * chunk;
-      const long long end = min(beg + chunk, (long long)T);
+      const long long end = p.fill ? min(beg + chunk, (long long)T) : beg;
       const float fv = bad ? nanf_() : -INFINITY;
       const float4 v4 = make_float4(fv, fv, fv, fv);
       const int nthr = n_mine == 0 ? kDecThreads : 128;
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     }
     __syncthreads();
     const long long R = gridDim.x, k = blockIdx.x;
-    const long long N = Pv[B], F = Pf[B];
+    const long long N = Pv[B], F = p.fill ? Pf[B] : 0;
     const int u0 = (int)(k * N / R), u1 = (int)((k + 1) * N / R);
     const int f0 = (int)(k * F / R), f1 = (int)((k + 1) * F / R);
 

@@ -9,6 +9,9 @@
 namespace dsa {
 cudaError_t launch_decode(const RowsParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream);
+cudaError_t launch_topk(const float* logits, long long ld, const int* seqlens, int rows, int T,
+                        int k, int* idx, float* vals, long long out_stride, int* status,
+                        cudaStream_t stream);
 cudaError_t launch_store(const uint16_t* k, const int* slots, int n, uint8_t* kcache,
                          long long page_stride, int num_pages, int kv_dtype, int* status,
                          cudaStream_t stream);
@@ -63,6 +66,7 @@ int check_and_pack(const void* q, const float* w, const void* kcache,
   p->out = out;
   p->out_stride = out_stride;
   p->status = dev_status;
+  p->fill = 1;
   return DSA_OK;
 }
 
@@ -114,6 +118,33 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
     if (n_q > 65535) return DSA_ERR_UNSUPPORTED;
     e = dsa::launch_decode(p, static_cast<cudaStream_t>(stream));
   }
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
+                            const void* kscale, long long page_stride_bytes, int num_pages,
+                            int kv_dtype, const int* block_table, long long bt_stride,
+                            const int* seqlens, int B, int H, int D, int page_size, int W,
+                            int k_top, int* topk_idx, float* topk_val, long long topk_stride,
+                            float* workspace, long long workspace_floats, int* dev_status,
+                            void* stream) {
+  dsa::RowsParams p;
+  const long long T = (long long)W * dsa::kPage;
+  int st = check_and_pack(q, w, kcache, kscale, page_stride_bytes, num_pages, kv_dtype,
+                          block_table, bt_stride, seqlens, B, H, D, page_size, W, workspace, T,
+                          dev_status, &p);
+  if (st != DSA_OK) return st;
+  if (k_top < 1 || !topk_idx || topk_stride < k_top) return DSA_ERR_INVALID_ARG;
+  if (B > 0 && workspace_floats < (long long)B * T) return DSA_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || (topk_val && !aligned(topk_val, 4))) return DSA_ERR_MISALIGNED;
+  if (B == 0) return DSA_OK;
+  if (B > 65535) return DSA_ERR_UNSUPPORTED;
+  p.fill = 0;      // the selection reads only t < L
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = dsa::launch_decode(p, s);
+  if (e == cudaSuccess)
+    e = dsa::launch_topk(workspace, T, seqlens, B, (int)T, k_top, topk_idx, topk_val, topk_stride,
+                         dev_status, s);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

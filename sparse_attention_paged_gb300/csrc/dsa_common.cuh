@@ -31,6 +31,8 @@ struct RowsParams {
   float* out;                  // row r at out + r * out_stride
   long long out_stride;
   int* status;                 // nullable
+  int fill;                    // decode: 1 = write the -inf past each row's last valid
+                               // page; 0 = leave it (top-k reads only t < L)
 };
 
 __device__ __forceinline__ void raise_status(int* status, int code) {

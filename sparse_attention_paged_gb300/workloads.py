@@ -49,7 +49,7 @@ POISON_F32 = 0x7FC00000                 # fp32 quiet NaN
 class Workload:
     """One call's worth of inputs, host-resident (numpy)."""
     name: str
-    kind: str                   # "decode" or "prefill"
+    kind: str                   # "decode", "prefill" or "topk" (decode + top-k selection)
     kv_dtype: int               # KV_E4M3 or KV_BF16
     R: int                      # rows: requests (decode) or queries (prefill)
     W: int                      # block-table width in pages
@@ -95,7 +95,10 @@ class Workload:
             key_bytes = int(L.sum()) * per_pos
             bt_bytes = int(np.ceil(L / self.P).sum()) * 4
         row_bytes = self.R * (H * D * 2 + H * 4 + 4)
-        out_bytes = self.R * self.W * self.P * 4
+        if self.kind == "topk":      # k positions and their logits per row
+            out_bytes = self.R * self.meta["k_top"] * 8
+        else:
+            out_bytes = self.R * self.W * self.P * 4
         return key_bytes + bt_bytes + row_bytes + out_bytes
 
     def flops(self) -> int:
@@ -386,6 +389,17 @@ def cfg8() -> StoreWorkload:
     return store_rows("store_fp8_n65536", 65536, 2048, seed=0)
 
 
+def cfg9() -> Workload:
+    """Config 3's decode call (fp8, B=64, W=4097) with top-2048 selection:
+    the positions and logits of each request's 2,048 best positions instead
+    of the [64, 262,208] logits."""
+    w = cfg3(4097)
+    w.name = "decode_topk2048_fp8_B64_W4097"
+    w.kind = "topk"
+    w.meta["k_top"] = 2048
+    return w
+
+
 def cfg6() -> Workload:
     """Prefill bf16, four requests in one call with per-query table rows:
     (query tokens, context) = (256, 6144), (512, 12288), (128, 3072),
@@ -412,4 +426,5 @@ NAMED = {
     "6": lambda: [cfg6()],
     "7": lambda: [cfg7()],
     "8": lambda: [cfg8()],
+    "9": lambda: [cfg9()],
 }

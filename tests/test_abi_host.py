@@ -119,3 +119,29 @@ def test_store_rejects_bad_arguments(lib, kw, code):
 @needs_nvcc
 def test_store_zero_rows_is_a_no_op(lib):
     assert store_call(n=0) == 0
+
+
+def topk_call(**kw):
+    import sparse_attention_paged_gb300 as s
+    args = dict(q=A, w=A, kcache=A, kscale=A + 8192, page_stride_bytes=8448, num_pages=16,
+                kv_dtype=0, block_table=A, bt_stride=8, seqlens=A, B=2, H=64, D=128,
+                page_size=64, W=8, k_top=64, topk_idx=A, topk_val=A, topk_stride=64,
+                workspace=A, workspace_floats=2 * 8 * 64, dev_status=None, stream=0)
+    args.update(kw)
+    return s.dsa_indexer_topk_decode(**args)
+
+
+@needs_nvcc
+@pytest.mark.parametrize("kw,code", [
+    (dict(k_top=0), 1), (dict(topk_idx=None), 1), (dict(topk_stride=63), 1),
+    (dict(workspace_floats=2 * 8 * 64 - 1), 1), (dict(workspace=None), 1),
+    (dict(topk_idx=A + 2), 3), (dict(topk_val=A + 1), 3), (dict(workspace=A + 4), 3),
+    (dict(H=32), 2), (dict(B=70000, workspace_floats=70000 * 512), 2),
+])
+def test_topk_rejects_bad_arguments(lib, kw, code):
+    assert topk_call(**kw) == code
+
+
+@needs_nvcc
+def test_topk_zero_rows_is_a_no_op(lib):
+    assert topk_call(B=0) == 0

@@ -1,0 +1,88 @@
+"""GPU parity of decode with top-k selection, through the C ABI, against the
+oracle's fp64 logits.  Positions whose logits sit within the parity
+tolerance of the k-th largest may be ordered either way, so the check is
+that the selection is a valid top-k: every selected position's oracle logit
+is at least the k-th largest minus the tolerance, every unselected valid
+position's at most it plus the tolerance; the returned values match the
+oracle's; positions are distinct, increasing and valid."""
+import numpy as np
+import pytest
+
+from sparse_attention_paged_gb300 import workloads as wl
+from tests.parity import REL_TOL, DeviceWorkload, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _topk(w, k, rows=None):
+    import torch
+    import sparse_attention_paged_gb300 as lib
+    dw = DeviceWorkload(w)
+    T = w.W * w.P
+    idx = torch.full((w.R, k), -7, dtype=torch.int32, device="cuda")
+    val = torch.full((w.R, k), 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(w.R * T, dtype=torch.float32, device="cuda")
+    st = lib.dsa_indexer_topk_decode(dw.q, dw.wt, dw.kcache, dw.kscale_ptr, w.page_stride,
+                                     w.num_pages, w.kv_dtype, dw.bt, w.bt_stride, dw.seqlens,
+                                     w.R, 64, 128, 64, w.W, k, idx, val, k, ws, ws.numel(),
+                                     dw.status)
+    assert st == 0
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), val.cpu().numpy(), int(dw.status.item())
+
+
+def _check(w, k, idx, val, rows):
+    ref, _ = oracle_rows(w, rows)
+    T = w.W * w.P
+    for j, r in enumerate(rows):
+        L = int(w.seqlens[r])
+        ir, vr = idx[r], val[r]
+        if L > T:                                    # an over-long row selects nothing
+            assert (ir == -1).all() and np.isneginf(vr).all()
+            continue
+        L = max(L, 0)
+        n = min(k, L)
+        assert (ir[n:] == -1).all() and np.isneginf(vr[n:]).all()
+        sel = ir[:n]
+        assert (np.diff(sel) > 0).all() and (sel >= 0).all() and (sel < L).all()
+        v = ref[j, :L]
+        if L == 0:
+            continue
+        tol = REL_TOL * float(np.abs(v).max())
+        assert np.abs(vr[:n] - v[sel]).max() <= tol
+        if L <= k:
+            assert np.array_equal(sel, np.arange(L))
+            continue
+        thr = np.sort(v)[::-1][k - 1]
+        mask = np.ones(L, bool)
+        mask[sel] = False
+        assert v[sel].min() >= thr - tol, (r, v[sel].min(), thr)
+        assert v[mask].max() <= thr + tol, (r, v[mask].max(), thr)
+
+
+@pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
+@pytest.mark.parametrize("k", [1, 64, 300])
+@pytest.mark.parametrize("W", [40, 90])             # per-request and balanced decode modes
+def test_topk_small(kv, k, W):
+    T = W * 64
+    lens = [0, 1, 63, k, k + 1, 700, T - 1, T, 2 * k]
+    w = wl.decode_with_lengths(f"tk{k}", lens, W, seed=12 + k, kv_dtype=kv)
+    idx, val, st = _topk(w, k)
+    assert st == 0
+    _check(w, k, idx, val, list(range(w.R)))
+
+
+def test_topk_over_long_row():
+    w = wl.decode_with_lengths("tk_bad", [100, 3 * 64 + 5, 5000 % 192], 3, seed=13)
+    idx, val, st = _topk(w, 16)
+    assert st == 7
+    _check(w, 16, idx, val, [0, 1, 2])
+
+
+def test_topk_config3_sampled_rows():
+    w = wl.cfg3(4097)
+    idx, val, st = _topk(w, 2048)
+    assert st == 0
+    L = w.seqlens
+    rows = sorted(set([int(np.argmin(L)), int(np.argmax(L)), 0, 1, 17, 63]))
+    _check(w, 2048, idx, val, rows)
