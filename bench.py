@@ -479,8 +479,9 @@ def run_ours(args, rank, world, local_rank):
         "gb_per_s": K * step_bytes / (elapsed_ms / 1e3) / 1e9,
         "roofline": roof,
         "clocks": sampler.summary(t_wall0, t_wall1),
-        "gpu_launches": K * len(works),
-        "gpu_launches_kernel_region": dom_launches,
+        # a top-k call is two kernels (logits, then the selection)
+        "gpu_launches": K * sum(2 if w.kind == "topk" else 1 for w in works),
+        "gpu_launches_kernel_region": dom_launches * (2 if dom.kind == "topk" else 1),
     }
 
     if not args.no_e2e:
