@@ -173,6 +173,26 @@ int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
                             void* stream);
 
 /*
+ * dsa_indexer_topk_decode without a caller workspace: the logits go to a
+ * fixed device array of the library (24 Mi floats, 96 MiB, held by the
+ * process once this entry point is first used).  Nothing is allocated by
+ * the call.  B * W * 64 must not exceed 24 Mi (DSA_ERR_UNSUPPORTED
+ * otherwise, checked before any device work).  The array is shared: calls
+ * on one device must not overlap (use one stream, or order the streams);
+ * the first call on a device looks up the array's address (which may load
+ * its module), so make one call before capturing one in a CUDA graph.  The
+ * pages have no counterpart: this is a convenience of the library.  Other
+ * arguments and results as for dsa_indexer_topk_decode.
+ */
+int dsa_indexer_topk_decode_static(const void* q, const float* w, const void* kcache,
+                                   const void* kscale, long long page_stride_bytes,
+                                   int num_pages, int kv_dtype, const int* block_table,
+                                   long long bt_stride, const int* seqlens, int B, int H, int D,
+                                   int page_size, int W, int k_top, int* topk_idx,
+                                   float* topk_val, long long topk_stride, int* dev_status,
+                                   void* stream);
+
+/*
  * Key-cache store: writes n new key rows into their cache slots, in the
  * page layouts above (the step before the indexer: its keys come from this
  * cache).  k: bf16 [n, 128], 16-byte aligned.  slot_mapping: int32 [n],

@@ -97,6 +97,18 @@ def dsa_indexer_topk_decode(q, w, kcache, kscale, page_stride_bytes, num_pages, 
         _p(workspace), int(workspace_floats), _p(dev_status), _stream(stream)))
 
 
+def dsa_indexer_topk_decode_static(q, w, kcache, kscale, page_stride_bytes, num_pages,
+                                   kv_dtype, block_table, bt_stride, seqlens, B, H, D,
+                                   page_size, W, k_top, topk_idx, topk_val, topk_stride,
+                                   dev_status=None, stream=None) -> int:
+    """C ``dsa_indexer_topk_decode_static``; returns its status code."""
+    return int(_native.load().dsa_indexer_topk_decode_static(
+        _p(q), _p(w), _p(kcache), _p(kscale), int(page_stride_bytes), int(num_pages),
+        int(kv_dtype), _p(block_table), int(bt_stride), _p(seqlens), int(B), int(H), int(D),
+        int(page_size), int(W), int(k_top), _p(topk_idx), _p(topk_val), int(topk_stride),
+        _p(dev_status), _stream(stream)))
+
+
 def dsa_kcache_store(k, slot_mapping, n, kcache, page_stride_bytes, num_pages, kv_dtype,
                      D, page_size, dev_status=None, stream=None) -> int:
     """C ``dsa_kcache_store``; returns its status code."""

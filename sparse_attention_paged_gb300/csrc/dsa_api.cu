@@ -12,6 +12,8 @@ cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream);
 cudaError_t launch_topk(const float* logits, long long ld, const int* seqlens, int rows, int T,
                         int k, int* idx, float* vals, long long out_stride, int* status,
                         cudaStream_t stream);
+long long static_scratch_floats();
+cudaError_t static_scratch(float** ptr);
 cudaError_t launch_store(const uint16_t* k, const int* slots, int n, uint8_t* kcache,
                          long long page_stride, int num_pages, int kv_dtype, int* status,
                          cudaStream_t stream);
@@ -146,6 +148,25 @@ int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
     e = dsa::launch_topk(workspace, T, seqlens, B, (int)T, k_top, topk_idx, topk_val, topk_stride,
                          dev_status, s);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_indexer_topk_decode_static(const void* q, const float* w, const void* kcache,
+                                   const void* kscale, long long page_stride_bytes,
+                                   int num_pages, int kv_dtype, const int* block_table,
+                                   long long bt_stride, const int* seqlens, int B, int H, int D,
+                                   int page_size, int W, int k_top, int* topk_idx,
+                                   float* topk_val, long long topk_stride, int* dev_status,
+                                   void* stream) {
+  // size first: an oversized call is refused before any device work
+  if (B < 0 || W < 1) return DSA_ERR_INVALID_ARG;
+  if ((long long)B * W * dsa::kPage > dsa::static_scratch_floats()) return DSA_ERR_UNSUPPORTED;
+  if (B == 0) return DSA_OK;
+  float* ws = nullptr;
+  if (dsa::static_scratch(&ws) != cudaSuccess) return DSA_ERR_CUDA;
+  return dsa_indexer_topk_decode(q, w, kcache, kscale, page_stride_bytes, num_pages, kv_dtype,
+                                 block_table, bt_stride, seqlens, B, H, D, page_size, W, k_top,
+                                 topk_idx, topk_val, topk_stride, ws,
+                                 dsa::static_scratch_floats(), dev_status, stream);
 }
 
 int dsa_kcache_store(const void* k, const int* slot_mapping, int n, void* kcache,

@@ -1,0 +1,102 @@
+"""The top-k entry point that allocates nothing (its logits go to a fixed
+device array of the library).  Collected last: its first GPU call loads the
+array's module and reserves the array for the rest of the process.
+
+Host part: the entry point is exported and refuses an oversized call before
+any device work.  GPU part: results bit-identical to the workspace entry
+point, and no device memory taken by repeated calls."""
+import os
+import shutil
+
+import numpy as np
+import pytest
+
+from sparse_attention_paged_gb300 import _native
+from sparse_attention_paged_gb300 import workloads as wl
+
+needs_nvcc = pytest.mark.skipif(shutil.which(_native.NVCC) is None and
+                                not os.path.exists(_native.LIB_PATH),
+                                reason="nvcc not available and library not built")
+A = 0x10000
+MAX_FLOATS = 24 << 20
+
+
+def _call(lib, **kw):
+    import sparse_attention_paged_gb300 as s
+    args = dict(q=A, w=A, kcache=A, kscale=A + 8192, page_stride_bytes=8448, num_pages=16,
+                kv_dtype=0, block_table=A, bt_stride=8, seqlens=A, B=2, H=64, D=128,
+                page_size=64, W=8, k_top=64, topk_idx=A, topk_val=A, topk_stride=64,
+                dev_status=None, stream=0)
+    args.update(kw)
+    return s.dsa_indexer_topk_decode_static(**args)
+
+
+@needs_nvcc
+def test_exported():
+    lib = _native.load()
+    assert hasattr(lib, "dsa_indexer_topk_decode_static")
+    assert "dsa_indexer_topk_decode_static" in _native.EXPORTS
+
+
+@needs_nvcc
+def test_oversized_call_is_refused_before_device_work():
+    lib = _native.load()
+    # 64 rows x 6,145 pages x 64 positions > 24 Mi floats; fake pointers:
+    # nothing may be touched
+    assert _call(lib, B=64, W=6145, bt_stride=6145) == 2
+    assert _call(lib, B=0) == 0
+    assert _call(lib, B=-1) == 1
+
+
+def _run_both(w, k):
+    import torch
+    import sparse_attention_paged_gb300 as lib
+    from tests.parity import DeviceWorkload
+    dw = DeviceWorkload(w)
+    T = w.W * w.P
+    outs = []
+    for static in (False, True):
+        idx = torch.full((w.R, k), -7, dtype=torch.int32, device="cuda")
+        val = torch.full((w.R, k), 7.0, dtype=torch.float32, device="cuda")
+        args = (dw.q, dw.wt, dw.kcache, dw.kscale_ptr, w.page_stride, w.num_pages, w.kv_dtype,
+                dw.bt, w.bt_stride, dw.seqlens, w.R, 64, 128, 64, w.W, k, idx, val, k)
+        if static:
+            st = lib.dsa_indexer_topk_decode_static(*args, dw.status)
+        else:
+            ws = torch.empty(w.R * T, dtype=torch.float32, device="cuda")
+            st = lib.dsa_indexer_topk_decode(*args, ws, ws.numel(), dw.status)
+        assert st == 0
+        torch.cuda.synchronize()
+        outs.append((idx.cpu().numpy(), val.cpu().numpy()))
+    return dw, outs
+
+
+@pytest.mark.gpu
+def test_static_matches_the_workspace_call():
+    for w, k in [(wl.decode_with_lengths("na", [0, 5, 700, 2000], 40, seed=21), 64),
+                 (wl.cfg3(4097), 2048)]:
+        _, ((i0, v0), (i1, v1)) = _run_both(w, k)
+        assert np.array_equal(i0, i1)
+        assert np.array_equal(v0.view(np.uint32), v1.view(np.uint32))
+
+
+@pytest.mark.gpu
+def test_repeated_calls_take_no_device_memory():
+    import torch
+    import sparse_attention_paged_gb300 as lib
+    from tests.parity import DeviceWorkload
+    w = wl.decode_with_lengths("na2", [100, 3000, 64], 60, seed=22)
+    dw = DeviceWorkload(w)
+    k = 32
+    idx = torch.empty((w.R, k), dtype=torch.int32, device="cuda")
+    val = torch.empty((w.R, k), dtype=torch.float32, device="cuda")
+    args = (dw.q, dw.wt, dw.kcache, dw.kscale_ptr, w.page_stride, w.num_pages, w.kv_dtype,
+            dw.bt, w.bt_stride, dw.seqlens, w.R, 64, 128, 64, w.W, k, idx, val, k, dw.status)
+    assert lib.dsa_indexer_topk_decode_static(*args) == 0      # first call: the array is set up
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(5):
+        assert lib.dsa_indexer_topk_decode_static(*args) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert int(dw.status.item()) == 0
