@@ -8,12 +8,18 @@
 // One CTA per row.  Logits become order-preserving 32-bit keys (a larger
 // float gives a larger key; NaN, which only an error row holds, the smallest
 // key).  A histogram of 2,048 linear bins over the row's range finds the bin
-// of the k-th largest logit, and a three-pass radix select (11 + 11 + 10
-// bits, shared-memory histograms) within that bin finds the k-th largest key
-// K* and how many keys equal to it are needed.  A last pass writes, in position order, every position whose
-// key is above K* and the first needed ones equal to it.  Rows of at most k
-// valid positions take all of them; the rest of the k outputs is -1 (value
-// -inf).
+// of the k-th largest logit; one more pass over the row collects that bin's
+// members into shared memory (usually a handful) and counts, per warp, the
+// positions in higher bins; a three-pass radix select (11 + 11 + 10 bits)
+// over the collected keys then finds the k-th largest key K* and how many
+// keys equal to it are needed.  (A bin too full to collect is resolved by
+// the same radix passes over the whole row.)  A last pass writes, in
+// position order, every position whose key is above K* and the first needed
+// ones equal to it.  Each warp owns a contiguous segment of the row, its
+// lanes on consecutive float4s, so that shared-memory reads are free of bank
+// conflicts and in-order output offsets come from warp ballots.  Rows of at
+// most k valid positions take all of them; the rest of the k outputs is -1
+// (value -inf).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -28,6 +34,10 @@ namespace {
 
 constexpr int kTkThreads = 1024;
 constexpr int kTkWarps = kTkThreads / 32;
+static_assert(kTkWarps == 32, "the per-warp scans run on one warp's lanes");
+constexpr int kCand = 2048;                  // keys of the k-th largest's bin kept for the exact passes
+constexpr int kRankMax = 128;                // at most this many collected keys: ranked directly
+constexpr int kStaticSmemReserve = 24 * 1024;  // the kernel's static shared arrays fit in this
 
 struct TopkParams {
   const float* logits;   // row r at logits + r * ld, positions [0, L_r) valid
@@ -80,9 +90,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* ws, int& total) 
 // Finds the bin holding the need-th largest entry of hist[0, nbins) counted
 // from the top (nbins <= 2 * kTkThreads): every thread takes two bins, a
 // block scan from the top gives each its count above; returns the bin and
-// writes the count above it to *above.
+// writes the count above it to *above and its own count to *pop.
 __device__ __forceinline__ int find_bin(const uint32_t* hist, int nbins, int need, int* ws,
-                                        int* sh_pick, int* above) {
+                                        int* sh_pick, int* above, int* pop) {
   const int t = threadIdx.x;
   const int b1 = nbins - 1 - 2 * t, b0 = b1 - 1;             // this thread's bins, high first
   const int h1 = b1 >= 0 ? (int)hist[b1] : 0;
@@ -92,24 +102,48 @@ __device__ __forceinline__ int find_bin(const uint32_t* hist, int nbins, int nee
   if (before < need && before + h1 >= need) {
     sh_pick[0] = b1;
     sh_pick[1] = before;
+    sh_pick[2] = h1;
   } else if (before + h1 < need && before + h1 + h0 >= need) {
     sh_pick[0] = b0;
     sh_pick[1] = before + h1;
+    sh_pick[2] = h0;
   }
   __syncthreads();
   *above = sh_pick[1];
+  *pop = sh_pick[2];
   const int bin = sh_pick[0];
   __syncthreads();
   return bin;
+}
+
+// Warp prefix of a per-lane count in 0..7: the lanes below this one, and
+// the warp's total.
+__device__ __forceinline__ int warp_prefix(int c, int lane, int& total) {
+  const uint32_t b0 = __ballot_sync(0xffffffffu, c & 1);
+  const uint32_t b1 = __ballot_sync(0xffffffffu, c & 2);
+  const uint32_t b2 = __ballot_sync(0xffffffffu, c & 4);
+  const uint32_t lt = (1u << lane) - 1u;
+  total = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+  return __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
 }
 
 __global__ void __launch_bounds__(kTkThreads)
     topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) float row_s[];             // the row, when it fits
   __shared__ uint32_t hist[2048];
+  __shared__ uint32_t cand_key[kCand];
+  __shared__ uint8_t cand_w[kCand];                           // the warp whose segment holds it
   __shared__ int ws[kTkWarps];
-  __shared__ int sh_pick[2];
+  __shared__ int sh_pick[3];
   __shared__ float red[2][kTkWarps];
+  __shared__ int w_gt[kTkWarps], w_eq[kTkWarps], w_out[kTkWarps], w_take[kTkWarps];
+  __shared__ int n_cand;
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the logits were written by the previous launch
   sm100::griddep_wait();
@@ -129,33 +163,59 @@ __global__ void __launch_bounds__(kTkThreads)
     return;
   }
 
-  // ---- the row into shared memory (if it fits), with its range (NaN, an
-  // error row's logit, is left out of the range)
-  const bool cached = L <= p.cache_floats;
-  const int L4 = L / 4;
-  float mn = INFINITY, mx = -INFINITY;
-  {
-    const float4* gr4 = reinterpret_cast<const float4*>(grow);    // rows are 256-byte aligned
-    for (int i4 = tid; i4 < L4; i4 += 4 * kTkThreads) {
+  // Warp w owns float4s [w_beg, w_end) of the row; the last float4 may run
+  // past L (still inside the row's T >= L floats, or the shared cache, both
+  // multiples of 4), and its positions >= L are masked everywhere.
+  const int n4 = (L + 3) >> 2;
+  const int seg4 = (n4 + kTkWarps - 1) / kTkWarps;
+  const int w_beg = min(n4, warp * seg4), w_end = min(n4, w_beg + seg4);
+  const bool cached = 4 * n4 <= p.cache_floats;
+  float4* s4 = reinterpret_cast<float4*>(row_s);
+  const float4* g4 = reinterpret_cast<const float4*>(grow);    // rows are 256-byte aligned
+  auto ld4 = [&](int j) -> float4 { return cached ? s4[j] : __ldcg(g4 + j); };
+  // valid positions in float4 j (0 past the warp's segment)
+  auto nvalid = [&](int j) { return j < w_end ? min(4, L - 4 * j) : 0; };
+  // every float4 of the warp's segment, four 16-byte loads in flight; fn runs
+  // on all lanes of a step (nvalid 0 on the idle ones) so that it may use
+  // warp votes; steps wholly past the segment are skipped
+  auto visit = [&](auto&& fn) {
+    for (int j0 = w_beg; j0 < w_end; j0 += 4 * 32) {
       float4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int j = i4 + u * kTkThreads;
-        v[u] = j < L4 ? __ldcg(gr4 + j) : make_float4(NAN, NAN, NAN, NAN);
+        const int j = j0 + u * 32 + lane;
+        v[u] = j < w_end ? ld4(j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = i4 + u * kTkThreads;
-        if (cached && j < L4) reinterpret_cast<float4*>(row_s)[j] = v[u];
-        mn = fminf(mn, fminf(fminf(v[u].x, v[u].y), fminf(v[u].z, v[u].w)));
-        mx = fmaxf(mx, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
-      }
+      for (int u = 0; u < 4; ++u)
+        if (j0 + u * 32 < w_end) fn(j0 + u * 32 + lane, v[u]);   // warp-uniform
     }
-    for (int i = 4 * L4 + tid; i < L; i += kTkThreads) {
-      const float x = grow[i];
-      if (cached) row_s[i] = x;
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
+  };
+
+  // ---- the row into shared memory (if it fits), with its range (NaN, an
+  // error row's logit, is left out of the range)
+  float mn = INFINITY, mx = -INFINITY;
+  for (int j0 = w_beg; j0 < w_end; j0 += 8 * 32) {          // eight 16-byte loads in flight
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u * 32 + lane;
+      v[u] = j < w_end ? __ldcg(g4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u * 32 + lane;
+      const int nv = nvalid(j);
+      if (nv == 0) continue;
+      if (cached) s4[j] = v[u];
+      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (e < nv) {
+          mn = fminf(mn, x[e]);
+          mx = fmaxf(mx, x[e]);
+        }
+      }
     }
   }
 #pragma unroll
@@ -167,6 +227,8 @@ __global__ void __launch_bounds__(kTkThreads)
     red[0][warp] = mn;
     red[1][warp] = mx;
   }
+  for (int b = tid; b < 2048; b += kTkThreads) hist[b] = 0;
+  if (tid == 0) n_cand = 0;
   __syncthreads();
   mn = INFINITY;
   mx = -INFINITY;
@@ -175,124 +237,239 @@ __global__ void __launch_bounds__(kTkThreads)
     mn = fminf(mn, red[0][w8]);
     mx = fmaxf(mx, red[1][w8]);
   }
-  const float* row = cached ? row_s : grow;             // scalar reads: generic loads
-  const float4* s4 = reinterpret_cast<const float4*>(row_s);
-  const float4* g4 = reinterpret_cast<const float4*>(grow);
-  auto ld4 = [&](int j) -> float4 { return cached ? s4[j] : __ldcg(g4 + j); };
 
-  // ---- the k-th largest key.  Logits crowd into a few sign/exponent
+  // ---- the bin of the k-th largest.  Logits crowd into a few sign/exponent
   // values, so a first radix digit would pile the histogram's atomics onto a
   // few bins.  The first pass instead bins linearly between the row's
   // smallest and largest logit (monotone in the logit, so the bin holding the
-  // k-th largest, and the count above it, are exact); three radix passes
-  // (11 + 11 + 10 bits of the key) then run over that bin's members.  NaN
-  // goes to bin 0 with key 0, the smallest.  An infinite or zero range puts
-  // everything in bin 0 (still exact).
+  // k-th largest, and the count above it, are exact).  NaN goes to bin 0
+  // with key 0, the smallest.  An infinite or zero range puts everything in
+  // bin 0 (still exact).
   const float span = mx - mn;
   const float inv = (span > 0.f && span < INFINITY) ? 2048.f / span : 0.f;
   auto lbin = [&](float x) -> int {
     if (!(x == x)) return 0;
     return min(2047, max(0, (int)((x - mn) * inv)));
   };
-  uint32_t prefix = 0, mask = 0;
+  visit([&](int j, float4 v) {
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    const int nv = nvalid(j);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < nv) atomicAdd(&hist[lbin(x[e])], 1u);
+  });
+  __syncthreads();
   int need = p.k;                            // entries still to take at or below the prefix
-  int lb = 0;                                // the chosen linear bin
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = pass == 1 ? 21 : pass == 2 ? 10 : 0;
-    const int nbins = pass == 3 ? 1024 : 2048;
-    for (int b = tid; b < nbins; b += kTkThreads) hist[b] = 0;
-    __syncthreads();
-    auto count = [&](float x) {
-      if (pass == 0) {
-        atomicAdd(&hist[lbin(x)], 1u);
-        return;
-      }
-      if (lbin(x) != lb) return;
-      const uint32_t key = order_key(x);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
-    };
-    for (int i4 = tid; i4 < L4; i4 += 4 * kTkThreads) {   // four 16-byte loads in flight
-      float4 v[4];
+  int above, pop;
+  const int lb = find_bin(hist, 2048, need, ws, sh_pick, &above, &pop);
+  need -= above;
+
+  // ---- the k-th largest key K* among the members of bin lb: the collected
+  // keys (ranked directly when few, else by radix passes), or the whole row
+  // by radix passes when the bin holds more than kCand of them
+  const bool collect = pop <= kCand;
+  int n_gt_bins = 0;                         // this lane's positions in bins above lb
+  if (collect) {
+    const uint32_t lt = (1u << lane) - 1u;
+    visit([&](int j, float4 v) {
+      const float x[4] = {v.x, v.y, v.z, v.w};
+      const int nv = nvalid(j);
+      bool c[4];
+      bool any = false;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = i4 + u * kTkThreads;
-        v[u] = j < L4 ? ld4(j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < 4; ++e) {
+        const int b = e < nv ? lbin(x[e]) : -1;
+        n_gt_bins += b > lb;
+        c[e] = b == lb;
+        any |= c[e];
       }
+      if (__ballot_sync(0xffffffffu, any) == 0u) return;   // warp-uniform: the usual case
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (i4 + u * kTkThreads >= L4) continue;
-        count(v[u].x);
-        count(v[u].y);
-        count(v[u].z);
-        count(v[u].w);
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t m = __ballot_sync(0xffffffffu, c[e]);
+        if (m) {                                          // warp-uniform
+          const int leader = __ffs(m) - 1;
+          int base = 0;
+          if (lane == leader) base = atomicAdd(&n_cand, __popc(m));
+          base = __shfl_sync(0xffffffffu, base, leader);
+          const int i = base + __popc(m & lt);
+          if (c[e] && i < kCand) {
+            cand_key[i] = order_key(x[e]);
+            cand_w[i] = (uint8_t)warp;
+          }
+        }
+      }
+    });
+  }
+  const int nc = min(pop, kCand);
+  uint32_t prefix = 0;
+  if (collect && nc <= kRankMax) {
+    // few keys: the need-th largest by direct ranking (thread i counts the
+    // keys above and equal to key i); every thread holding a copy of it
+    // writes the same pair
+    __syncthreads();                         // the collected keys are in place
+    if (tid < nc) {
+      const uint32_t key = cand_key[tid];
+      int gt = 0, eq = 0;
+      for (int i = 0; i < nc; ++i) {
+        const uint32_t o = cand_key[i];
+        gt += o > key;
+        eq += o == key;
+      }
+      if (gt < need && need <= gt + eq) {
+        sh_pick[0] = (int)key;
+        sh_pick[1] = gt;
       }
     }
-    for (int i = 4 * L4 + tid; i < L; i += kTkThreads) count(row[i]);   // the last L % 4
     __syncthreads();
-    int above;
-    const int bin = find_bin(hist, nbins, need, ws, sh_pick, &above);
-    if (pass == 0) {
-      lb = bin;
-    } else {
+    prefix = (uint32_t)sh_pick[0];
+    need -= sh_pick[1];
+  } else {
+    // three radix passes (11 + 11 + 10 bits)
+    uint32_t mask = 0;
+#pragma unroll 1
+    for (int pass = 1; pass < 4; ++pass) {
+      const int shift = pass == 1 ? 21 : pass == 2 ? 10 : 0;
+      const int nbins = pass == 3 ? 1024 : 2048;
+      __syncthreads();                       // the previous pass's hist reads are done
+      for (int b = tid; b < nbins; b += kTkThreads) hist[b] = 0;
+      __syncthreads();
+      if (collect) {
+        for (int i = tid; i < nc; i += kTkThreads) {
+          const uint32_t key = cand_key[i];
+          if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
+        }
+      } else {
+        visit([&](int j, float4 v) {
+          const float x[4] = {v.x, v.y, v.z, v.w};
+          const int nv = nvalid(j);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (e >= nv || lbin(x[e]) != lb) continue;
+            const uint32_t key = order_key(x[e]);
+            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
+          }
+        });
+      }
+      __syncthreads();
+      const int bin = find_bin(hist, nbins, need, ws, sh_pick, &above, &pop);
       prefix |= (uint32_t)bin << shift;
       mask |= (uint32_t)(nbins - 1) << shift;
+      need -= above;
     }
-    need -= above;
   }
   const uint32_t kstar = prefix;             // the k-th largest key; `need` of its copies are taken
 
-  // ---- selection, in position order: every key above K*, the first `need`
-  // equal to it.  Thread t scans a contiguous chunk of positions.
-  const int chunk = ((L + kTkThreads - 1) / kTkThreads + 3) & ~3;    // whole float4s
-  const int c0 = min(L, tid * chunk), c1 = min(L, c0 + chunk);
-  int n_gt = 0, n_eq = 0;
-  for (int i = c0; i < c1; i += 16) {       // four 16-byte loads in flight
-    float4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      v[u] = i + 4 * u + 3 < c1 ? ld4((i >> 2) + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+  // ---- per warp: positions above K*, and equal to it
+  if (collect) {
+    const int g = warp_sum(n_gt_bins);
+    if (lane == 0) {
+      w_gt[warp] = g;
+      w_eq[warp] = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < nc; i += kTkThreads) {
+      const uint32_t key = cand_key[i];
+      if (key > kstar) atomicAdd(&w_gt[cand_w[i]], 1);
+      else if (key == kstar) atomicAdd(&w_eq[cand_w[i]], 1);
+    }
+  } else {
+    int n_gt = 0, n_eq = 0;
+    visit([&](int j, float4 v) {
+      const float x[4] = {v.x, v.y, v.z, v.w};
+      const int nv = nvalid(j);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int pos = i + 4 * u + e;
-        if (pos >= c1) continue;
-        const uint32_t key = order_key(i + 4 * u + 3 < c1 ? x[e] : row[pos]);
+        if (e >= nv) continue;
+        const uint32_t key = order_key(x[e]);
         n_gt += key > kstar;
         n_eq += key == kstar;
       }
+    });
+    n_gt = warp_sum(n_gt);
+    n_eq = warp_sum(n_eq);
+    if (lane == 0) {
+      w_gt[warp] = n_gt;
+      w_eq[warp] = n_eq;
     }
   }
-  int tot;
-  const int eq_before = block_exclusive_scan(n_eq, ws, tot);
-  const int eq_take = max(0, min(n_eq, need - eq_before));
-  const int out0 = block_exclusive_scan(n_gt + eq_take, ws, tot);
-  const int o_end = out0 + n_gt + eq_take;
-  int o = out0, eq_seen = 0;
-  for (int i = c0; i < c1 && o < o_end; i += 16) {
+  __syncthreads();
+  // warp 0: the copies of K* each warp takes (the first `need` in position
+  // order) and each warp's first output slot
+  if (warp == 0) {
+    const int g = w_gt[lane], q = w_eq[lane];
+    int qs = q;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, qs, o);
+      if (lane >= o) qs += y;
+    }
+    const int take = max(0, min(q, need - (qs - q)));
+    int ts = g + take;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ts, o);
+      if (lane >= o) ts += y;
+    }
+    w_out[lane] = ts - (g + take);
+    w_take[lane] = take;
+  }
+  __syncthreads();
+
+  // ---- the selection, in position order: every key above K*, the first
+  // w_take[warp] equal to it
+  int o = w_out[warp];
+  const int o_end = o + w_gt[warp] + w_take[warp];
+  const int o_lim = min(o_end, p.k);         // the counts say o_end <= k; never write past k
+  const int eq_take = w_take[warp];
+  int eq_seen = 0;
+  for (int j0 = w_beg; j0 < w_end && o < o_end; j0 += 4 * 32) {   // warp-uniform
     float4 v[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      v[u] = i + 4 * u + 3 < c1 ? ld4((i >> 2) + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * 32 + lane;
+      v[u] = j < w_end ? ld4(j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
+      if (j0 + u * 32 >= w_end) break;       // warp-uniform: past the segment
+      const int j = j0 + u * 32 + lane;
       const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      bool gt[4], eq[4];
+      int c_eq = 0;
+      const int nv = nvalid(j);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int pos = i + 4 * u + e;
-        if (pos >= c1) continue;
-        const float val = i + 4 * u + 3 < c1 ? x[e] : row[pos];
-        const uint32_t key = order_key(val);
-        bool take = key > kstar;
-        if (key == kstar) take = eq_seen++ < eq_take;
-        if (take) {
-          orow[o] = pos;
-          if (vrow) vrow[o] = val;
-          ++o;
+        const uint32_t key = order_key(x[e]);
+        gt[e] = e < nv && key > kstar;
+        eq[e] = e < nv && key == kstar;
+        c_eq += eq[e];
+      }
+      int tot_eq = 0, rank = eq_seen;
+      if (__ballot_sync(0xffffffffu, c_eq != 0) != 0u)        // warp-uniform: a tie in this step
+        rank += warp_prefix(c_eq, lane, tot_eq);
+      bool take[4];
+      int c_take = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        take[e] = gt[e] || (eq[e] && rank < eq_take);
+        rank += eq[e];
+        c_take += take[e];
+      }
+      int tot_take;
+      int oo = o + warp_prefix(c_take, lane, tot_take);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (take[e]) {
+          if (oo < o_lim) {
+            orow[oo] = 4 * j + e;
+            if (vrow) vrow[oo] = x[e];
+          }
+          ++oo;
         }
       }
+      eq_seen += tot_eq;
+      o += tot_take;
     }
   }
 }
@@ -314,7 +491,7 @@ cudaError_t launch_topk(const float* logits, long long ld, const int* seqlens, i
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
         cudaSuccess)
       return e;
-    const int bytes = ((optin - 16 * 1024) / 16) * 16;      // leave room for the static arrays
+    const int bytes = ((optin - kStaticSmemReserve) / 16) * 16;   // room for the static arrays
     if ((e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   bytes)) != cudaSuccess)
       return e;
