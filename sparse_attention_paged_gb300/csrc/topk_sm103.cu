@@ -37,7 +37,9 @@ constexpr int kTkWarps = kTkThreads / 32;
 static_assert(kTkWarps == 32, "the per-warp scans run on one warp's lanes");
 constexpr int kCand = 2048;                  // keys of the k-th largest's bin kept for the exact passes
 constexpr int kRankMax = 128;                // at most this many collected keys: ranked directly
-constexpr int kStaticSmemReserve = 24 * 1024;  // the kernel's static shared arrays fit in this
+constexpr int kMaskSteps = 16;               // steps of 32 float4s per warp kept as vote masks
+static_assert(kTkWarps * kMaskSteps * 4 == 2048, "the vote masks take the histogram's place");
+constexpr int kStaticSmemReserve = 28 * 1024;  // the kernel's static shared arrays fit in this
 
 struct TopkParams {
   const float* logits;   // row r at logits + r * ld, positions [0, L_r) valid
@@ -136,9 +138,9 @@ __device__ __forceinline__ int warp_sum(int v) {
 __global__ void __launch_bounds__(kTkThreads)
     topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) float row_s[];             // the row, when it fits
-  __shared__ uint32_t hist[2048];
+  __shared__ __align__(16) uint32_t hist[2048];
   __shared__ uint32_t cand_key[kCand];
-  __shared__ uint8_t cand_w[kCand];                           // the warp whose segment holds it
+  __shared__ int cand_pos[kCand];
   __shared__ int ws[kTkWarps];
   __shared__ int sh_pick[3];
   __shared__ float red[2][kTkWarps];
@@ -192,29 +194,27 @@ __global__ void __launch_bounds__(kTkThreads)
     }
   };
 
-  // ---- the row into shared memory (if it fits), with its range (NaN, an
-  // error row's logit, is left out of the range)
+  // ---- the bins: 2,048 linear bins over the range of a sample (every
+  // lane's first float4), widened by an eighth of its span on each side.
+  // Logits crowd into a few sign/exponent values, so a first radix digit
+  // would pile the histogram's atomics onto a few bins; linear bins do not.
+  // Any binning monotone in the logit keeps the counts exact (values past
+  // the range land in the end bins), so the bin of the k-th largest and the
+  // count above it are exact; the sample only decides how crowded that bin
+  // is.  NaN (an error row's logit, left out of the range) goes to bin 0 with
+  // key 0, the smallest.  A zero or infinite range puts everything in bin 0
+  // (still exact).
+  const int j_first = w_beg + lane;
+  const float4 v_first = j_first < w_end ? __ldcg(g4 + j_first) : make_float4(0.f, 0.f, 0.f, 0.f);
   float mn = INFINITY, mx = -INFINITY;
-  for (int j0 = w_beg; j0 < w_end; j0 += 8 * 32) {          // eight 16-byte loads in flight
-    float4 v[8];
+  {
+    const int nv = nvalid(j_first);
+    const float x[4] = {v_first.x, v_first.y, v_first.z, v_first.w};
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int j = j0 + u * 32 + lane;
-      v[u] = j < w_end ? __ldcg(g4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int j = j0 + u * 32 + lane;
-      const int nv = nvalid(j);
-      if (nv == 0) continue;
-      if (cached) s4[j] = v[u];
-      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (e < nv) {
-          mn = fminf(mn, x[e]);
-          mx = fmaxf(mx, x[e]);
-        }
+    for (int e = 0; e < 4; ++e) {
+      if (e < nv) {
+        mn = fminf(mn, x[e]);
+        mx = fmaxf(mx, x[e]);
       }
     }
   }
@@ -237,27 +237,46 @@ __global__ void __launch_bounds__(kTkThreads)
     mn = fminf(mn, red[0][w8]);
     mx = fmaxf(mx, red[1][w8]);
   }
-
-  // ---- the bin of the k-th largest.  Logits crowd into a few sign/exponent
-  // values, so a first radix digit would pile the histogram's atomics onto a
-  // few bins.  The first pass instead bins linearly between the row's
-  // smallest and largest logit (monotone in the logit, so the bin holding the
-  // k-th largest, and the count above it, are exact).  NaN goes to bin 0
-  // with key 0, the smallest.  An infinite or zero range puts everything in
-  // bin 0 (still exact).
-  const float span = mx - mn;
+  float span = mx - mn, lo = mn;
+  if (span > 0.f && span < INFINITY) {
+    lo = mn - 0.125f * span;
+    span *= 1.25f;
+  }
   const float inv = (span > 0.f && span < INFINITY) ? 2048.f / span : 0.f;
   auto lbin = [&](float x) -> int {
     if (!(x == x)) return 0;
-    return min(2047, max(0, (int)((x - mn) * inv)));
+    return min(2047, max(0, (int)((x - lo) * inv)));
   };
-  visit([&](int j, float4 v) {
-    const float x[4] = {v.x, v.y, v.z, v.w};
+
+  // ---- one pass over the row: into shared memory (if it fits), the
+  // histogram, and each position's bin (16 bits, when the row and its bins
+  // fit)
+  const bool bins_cached = 6 * n4 <= p.cache_floats;
+  uint2* b2 = reinterpret_cast<uint2*>(row_s + 4 * n4);       // four bins per float4
+  auto bin_float4 = [&](int j, float4 v) {
     const int nv = nvalid(j);
+    if (nv == 0) return;
+    if (cached) s4[j] = v;
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    uint32_t bq[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (e < nv) atomicAdd(&hist[lbin(x[e])], 1u);
-  });
+    for (int e = 0; e < 4; ++e) {
+      bq[e] = (uint32_t)lbin(x[e]);
+      if (e < nv) atomicAdd(&hist[bq[e]], 1u);
+    }
+    if (bins_cached) b2[j] = make_uint2(bq[0] | (bq[1] << 16), bq[2] | (bq[3] << 16));
+  };
+  bin_float4(j_first, v_first);
+  for (int j0 = w_beg + 32; j0 < w_end; j0 += 8 * 32) {      // eight 16-byte loads in flight
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u * 32 + lane;
+      v[u] = j < w_end ? __ldcg(g4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) bin_float4(j0 + u * 32 + lane, v[u]);
+  }
   __syncthreads();
   int need = p.k;                            // entries still to take at or below the prefix
   int above, pop;
@@ -265,56 +284,119 @@ __global__ void __launch_bounds__(kTkThreads)
   need -= above;
 
   // ---- the k-th largest key K* among the members of bin lb: the collected
-  // keys (ranked directly when few, else by radix passes), or the whole row
-  // by radix passes when the bin holds more than kCand of them
+  // keys, or the whole row by radix passes when the bin holds more than
+  // kCand of them.
+  //
+  // The usual case ("fast": at most kRankMax members and a segment of at
+  // most kMaskSteps steps) ranks the collected keys directly and records
+  // the positions taken as warp-vote masks, one word per (warp, step,
+  // element of the float4), in the histogram's place (free once bin lb is
+  // known): positions in bins above lb while the row is collected, then the
+  // collected ones that make the cut.
   const bool collect = pop <= kCand;
+  const int S = (seg4 + 31) >> 5;            // steps of 32 float4s in a warp's segment
+  const bool fast = pop <= kRankMax && S <= kMaskSteps;
+  uint32_t* tmask = hist;
+  auto mask_word = [&](int w, int step, int e) -> uint32_t& {
+    return tmask[(w * kMaskSteps + step) * 4 + e];
+  };
+  if (fast) {                                // each warp clears its own words
+    for (int i = lane; i < kMaskSteps * 4; i += 32) tmask[warp * kMaskSteps * 4 + i] = 0u;
+    __syncwarp();
+  }
   int n_gt_bins = 0;                         // this lane's positions in bins above lb
-  if (collect) {
-    const uint32_t lt = (1u << lane) - 1u;
+  const uint32_t lt = (1u << lane) - 1u;
+  // one step of the collection: b[e] is the bin of position 4j+e (-1 past
+  // the segment); x_of() gives the float4, read only by lanes holding a
+  // member of bin lb
+  auto collect_step = [&](int j, const int (&b)[4], auto&& x_of) {
+    bool c[4], d[4];
+    bool any = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      d[e] = b[e] > lb;
+      n_gt_bins += d[e];
+      c[e] = b[e] == lb;
+      any |= c[e];
+    }
+    if (fast) {
+      const uint32_t m0 = __ballot_sync(0xffffffffu, d[0]);
+      const uint32_t m1 = __ballot_sync(0xffffffffu, d[1]);
+      const uint32_t m2 = __ballot_sync(0xffffffffu, d[2]);
+      const uint32_t m3 = __ballot_sync(0xffffffffu, d[3]);
+      if (lane < 4)
+        mask_word(warp, (j - lane - w_beg) >> 5, lane) =
+            lane == 0 ? m0 : lane == 1 ? m1 : lane == 2 ? m2 : m3;
+    }
+    if (__ballot_sync(0xffffffffu, any) == 0u) return;     // warp-uniform: the usual case
+    const float4 v = any ? x_of() : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t m = __ballot_sync(0xffffffffu, c[e]);
+      if (m) {                                            // warp-uniform
+        const int leader = __ffs(m) - 1;
+        int base = 0;
+        if (lane == leader) base = atomicAdd(&n_cand, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        const int i = base + __popc(m & lt);
+        if (c[e] && i < kCand) {
+          cand_key[i] = order_key(x[e]);
+          cand_pos[i] = 4 * j + e;
+        }
+      }
+    }
+  };
+  if (collect && bins_cached) {
+    for (int j0 = w_beg; j0 < w_end; j0 += 4 * 32) {       // four 8-byte loads in flight
+      uint2 bb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * 32 + lane;
+        bb[u] = j < w_end ? b2[j] : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (j0 + u * 32 >= w_end) break;                  // warp-uniform: past the segment
+        const int j = j0 + u * 32 + lane;
+        const int nv = nvalid(j);
+        int b[4] = {(int)(bb[u].x & 0xffffu), (int)(bb[u].x >> 16), (int)(bb[u].y & 0xffffu),
+                    (int)(bb[u].y >> 16)};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e >= nv) b[e] = -1;
+        collect_step(j, b, [&] { return s4[j]; });
+      }
+    }
+  } else if (collect) {
     visit([&](int j, float4 v) {
       const float x[4] = {v.x, v.y, v.z, v.w};
       const int nv = nvalid(j);
-      bool c[4];
-      bool any = false;
+      int b[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int b = e < nv ? lbin(x[e]) : -1;
-        n_gt_bins += b > lb;
-        c[e] = b == lb;
-        any |= c[e];
-      }
-      if (__ballot_sync(0xffffffffu, any) == 0u) return;   // warp-uniform: the usual case
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t m = __ballot_sync(0xffffffffu, c[e]);
-        if (m) {                                          // warp-uniform
-          const int leader = __ffs(m) - 1;
-          int base = 0;
-          if (lane == leader) base = atomicAdd(&n_cand, __popc(m));
-          base = __shfl_sync(0xffffffffu, base, leader);
-          const int i = base + __popc(m & lt);
-          if (c[e] && i < kCand) {
-            cand_key[i] = order_key(x[e]);
-            cand_w[i] = (uint8_t)warp;
-          }
-        }
-      }
+      for (int e = 0; e < 4; ++e) b[e] = e < nv ? lbin(x[e]) : -1;
+      collect_step(j, b, [&] { return v; });
     });
   }
   const int nc = min(pop, kCand);
-  uint32_t prefix = 0;
-  if (collect && nc <= kRankMax) {
-    // few keys: the need-th largest by direct ranking (thread i counts the
-    // keys above and equal to key i); every thread holding a copy of it
-    // writes the same pair
-    __syncthreads();                         // the collected keys are in place
+  auto warp_of = [&](int pos) { return (pos >> 2) / seg4; };
+  uint32_t kstar = 0;
+  if (fast) {
+    // thread i ranks collected key i: the keys above it, equal to it, and
+    // equal to it at a lower position; every thread holding a copy of the
+    // need-th largest writes the same pair
+    __syncthreads();                         // the collected keys and the masks are in place
+    uint32_t key = 0;
+    int pos = 0, eq_lower = 0;
     if (tid < nc) {
-      const uint32_t key = cand_key[tid];
+      key = cand_key[tid];
+      pos = cand_pos[tid];
       int gt = 0, eq = 0;
       for (int i = 0; i < nc; ++i) {
         const uint32_t o = cand_key[i];
         gt += o > key;
         eq += o == key;
+        eq_lower += o == key && cand_pos[i] < pos;
       }
       if (gt < need && need <= gt + eq) {
         sh_pick[0] = (int)key;
@@ -322,11 +404,23 @@ __global__ void __launch_bounds__(kTkThreads)
       }
     }
     __syncthreads();
-    prefix = (uint32_t)sh_pick[0];
-    need -= sh_pick[1];
+    kstar = (uint32_t)sh_pick[0];
+    need -= sh_pick[1];                      // copies of K* taken, lowest positions first
+    if (tid < nc && (key > kstar || (key == kstar && eq_lower < need))) {
+      const int j = pos >> 2, w = warp_of(pos), rel = j - w * seg4;
+      atomicOr(&mask_word(w, rel >> 5, pos & 3), 1u << (rel & 31));
+    }
+    __syncthreads();
+    int cnt = 0;
+    for (int i = lane; i < S * 4; i += 32) cnt += __popc(tmask[warp * kMaskSteps * 4 + i]);
+    cnt = warp_sum(cnt);
+    if (lane == 0) {
+      w_gt[warp] = cnt;
+      w_eq[warp] = 0;
+    }
   } else {
     // three radix passes (11 + 11 + 10 bits)
-    uint32_t mask = 0;
+    uint32_t prefix = 0, mask = 0;
 #pragma unroll 1
     for (int pass = 1; pass < 4; ++pass) {
       const int shift = pass == 1 ? 21 : pass == 2 ? 10 : 0;
@@ -357,40 +451,39 @@ __global__ void __launch_bounds__(kTkThreads)
       mask |= (uint32_t)(nbins - 1) << shift;
       need -= above;
     }
-  }
-  const uint32_t kstar = prefix;             // the k-th largest key; `need` of its copies are taken
-
-  // ---- per warp: positions above K*, and equal to it
-  if (collect) {
-    const int g = warp_sum(n_gt_bins);
-    if (lane == 0) {
-      w_gt[warp] = g;
-      w_eq[warp] = 0;
-    }
-    __syncthreads();
-    for (int i = tid; i < nc; i += kTkThreads) {
-      const uint32_t key = cand_key[i];
-      if (key > kstar) atomicAdd(&w_gt[cand_w[i]], 1);
-      else if (key == kstar) atomicAdd(&w_eq[cand_w[i]], 1);
-    }
-  } else {
-    int n_gt = 0, n_eq = 0;
-    visit([&](int j, float4 v) {
-      const float x[4] = {v.x, v.y, v.z, v.w};
-      const int nv = nvalid(j);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (e >= nv) continue;
-        const uint32_t key = order_key(x[e]);
-        n_gt += key > kstar;
-        n_eq += key == kstar;
+    kstar = prefix;                          // the k-th largest key; `need` of its copies are taken
+    // per warp: positions above K*, and equal to it
+    if (collect) {
+      const int g = warp_sum(n_gt_bins);
+      if (lane == 0) {
+        w_gt[warp] = g;
+        w_eq[warp] = 0;
       }
-    });
-    n_gt = warp_sum(n_gt);
-    n_eq = warp_sum(n_eq);
-    if (lane == 0) {
-      w_gt[warp] = n_gt;
-      w_eq[warp] = n_eq;
+      __syncthreads();
+      for (int i = tid; i < nc; i += kTkThreads) {
+        const uint32_t key = cand_key[i];
+        if (key > kstar) atomicAdd(&w_gt[warp_of(cand_pos[i])], 1);
+        else if (key == kstar) atomicAdd(&w_eq[warp_of(cand_pos[i])], 1);
+      }
+    } else {
+      int n_gt = 0, n_eq = 0;
+      visit([&](int j, float4 v) {
+        const float x[4] = {v.x, v.y, v.z, v.w};
+        const int nv = nvalid(j);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e >= nv) continue;
+          const uint32_t key = order_key(x[e]);
+          n_gt += key > kstar;
+          n_eq += key == kstar;
+        }
+      });
+      n_gt = warp_sum(n_gt);
+      n_eq = warp_sum(n_eq);
+      if (lane == 0) {
+        w_gt[warp] = n_gt;
+        w_eq[warp] = n_eq;
+      }
     }
   }
   __syncthreads();
@@ -416,11 +509,39 @@ __global__ void __launch_bounds__(kTkThreads)
   }
   __syncthreads();
 
-  // ---- the selection, in position order: every key above K*, the first
-  // w_take[warp] equal to it
+  // ---- the selection, in position order
   int o = w_out[warp];
   const int o_end = o + w_gt[warp] + w_take[warp];
   const int o_lim = min(o_end, p.k);         // the counts say o_end <= k; never write past k
+  if (fast) {
+    // from the masks: lane l's positions of a step follow those of lanes < l
+    const int steps = (w_end - w_beg + 31) >> 5;
+    for (int step = 0; step < steps && o < o_end; ++step) {        // warp-uniform
+      const uint4 m4 = *reinterpret_cast<const uint4*>(&mask_word(warp, step, 0));
+      const uint32_t M[4] = {m4.x, m4.y, m4.z, m4.w};
+      const int tot = __popc(M[0]) + __popc(M[1]) + __popc(M[2]) + __popc(M[3]);
+      if (tot == 0) continue;
+      if (((M[0] | M[1] | M[2] | M[3]) >> lane) & 1u) {
+        const int j = w_beg + step * 32 + lane;
+        int oo = o + __popc(M[0] & lt) + __popc(M[1] & lt) + __popc(M[2] & lt) + __popc(M[3] & lt);
+        const float4 v = ld4(j);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if ((M[e] >> lane) & 1u) {
+            if (oo < o_lim) {
+              orow[oo] = 4 * j + e;
+              if (vrow) vrow[oo] = x[e];
+            }
+            ++oo;
+          }
+        }
+      }
+      o += tot;
+    }
+    return;
+  }
+  // from the keys: every key above K*, the first w_take[warp] equal to it
   const int eq_take = w_take[warp];
   int eq_seen = 0;
   for (int j0 = w_beg; j0 < w_end && o < o_end; j0 += 4 * 32) {   // warp-uniform

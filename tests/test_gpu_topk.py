@@ -90,43 +90,56 @@ def test_topk_config3_sampled_rows():
 
 @pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
 def test_topk_ties_take_the_lowest_positions(kv):
-    """Rows whose k-th largest logit is shared by more positions than the
-    kernel collects: an all-zero query (every logit 0, so the first k
-    positions), and zeroed key pages under the first 3,008 positions of a
-    row (the k-th largest falls among those zeros)."""
-    W, k = 90, 2048
-    lens = [5000, 5000, 3000, 2049]
+    """Rows whose k-th largest logit is shared by many positions: an
+    all-zero query (every logit 0, so the first k positions); zeroed key
+    pages under the first 3,008 positions of a row (more copies of the k-th
+    value than the kernel collects); and zeroed pages under the first 512
+    positions of a row with k set so that the k-th largest is one of them
+    (collected, but too many to rank directly)."""
+    W, k = 120, 2048
+    lens = [5000, 5000, 3000, 2049, 7500]
     w = wl.decode_with_lengths("tk_ties", lens, W, seed=31, kv_dtype=kv)
     w.q_bits[0] = 0
     w.q_bits[3] = 0
-    n_zero_pages = 47                                  # 3,008 positions
-    for pg in w.block_table[1, :n_zero_pages]:
-        base = int(pg) * w.page_stride
-        w.kcache[base: base + (8192 if kv == wl.KV_E4M3 else 16384)] = 0
+    zero_pages = {1: 47, 4: 8}
+    for r, n in zero_pages.items():
+        for pg in w.block_table[r, :n]:
+            base = int(pg) * w.page_stride
+            w.kcache[base: base + (8192 if kv == wl.KV_E4M3 else 16384)] = 0
+    ref, _ = oracle_rows(w, [1, 4])
+
+    def zeros_taken_first(r, v, sel, k):
+        n_pos = int((v > 0).sum())
+        assert (v[:64 * zero_pages[r]] == 0).all()
+        assert n_pos < k <= n_pos + 64 * zero_pages[r]   # the k-th largest is a zero
+        # the zeros taken are the lowest-numbered ones (positions 0, 1, ...);
+        # a logit within rounding of 0 may trade places with a zero
+        taken = sel[v[sel] == 0]
+        assert np.array_equal(taken, np.arange(len(taken)))
+        assert abs(len(taken) - (k - n_pos)) <= 2
+
     idx, val, st = _topk(w, k)
     assert st == 0
     _check(w, k, idx, val, list(range(w.R)))
     for r in (0, 3):
         assert np.array_equal(idx[r], np.arange(k))
         assert (val[r] == 0).all()
-    ref, _ = oracle_rows(w, [1])
-    v = ref[0, :lens[1]]
-    assert (v[:64 * n_zero_pages] == 0).all()
-    n_pos = int((v > 0).sum())
-    assert n_pos < k <= n_pos + 64 * n_zero_pages        # the k-th largest is a zero
-    # the zeros taken are the lowest-numbered ones (positions 0, 1, ...); a
-    # logit within rounding of 0 may trade places with a zero
-    sel = idx[1]
-    zeros_taken = sel[v[sel] == 0]
-    assert np.array_equal(zeros_taken, np.arange(len(zeros_taken)))
-    assert abs(len(zeros_taken) - (k - n_pos)) <= 2
+    zeros_taken_first(1, ref[0, :lens[1]], idx[1], k)
+
+    v4 = ref[1, :lens[4]]
+    k4 = int((v4 > 0).sum()) + 256
+    idx, val, st = _topk(w, k4)
+    assert st == 0
+    _check(w, k4, idx, val, [4])
+    zeros_taken_first(4, v4, idx[4], k4)
 
 
 def test_topk_rows_longer_than_the_shared_cache():
-    """Rows past the shared-memory row cache (about 52K logits) are read
-    from global memory in every pass."""
-    W = 1000
-    lens = [60000, 52100, 3000, 64000]
+    """Rows past the shared-memory row cache (about 51K logits) are read
+    from global memory in every pass; past 65,536 the in-order write
+    evaluates every key."""
+    W = 1100
+    lens = [60000, 52100, 3000, 64000, 70000]
     w = wl.decode_with_lengths("tk_long", lens, W, seed=32)
     for k in (64, 2048):
         idx, val, st = _topk(w, k)
