@@ -51,13 +51,15 @@ WORKLOAD_DESC = {
     "5": "prefill bf16 n_q=4096 W=352 causal limit 18432+i",
     "6": "prefill bf16, 4 requests (query tokens, context) = (256, 6144), (512, 12288), "
          "(128, 3072), (1024, 20480), per-query table rows",
+    "6v": "prefill bf16, the same 4 requests, one table row per request (a query-tile launch "
+          "per request)",
     "7": "prefill fp8 n_q=1024 W=128 causal limit 7168+i",
     "8": "key-cache store: 65536 bf16 key rows into e4m3 pages (+ scales), random slots of 2048 pages",
     "9": "decode fp8 B=64 W=4097 L log-uniform 512..32768, top-2048 positions per request",
 }
 # default (steps, warmup): a timed region of roughly one second per GPU
 DEFAULT_STEPS = {"1": 100000, "2": 100000, "3": 20000, "3ref": 20000, "3short": 40000,
-                 "3short_capped": 100000, "4": 10000, "5": 1000, "6": 2000, "7": 5000,
+                 "3short_capped": 100000, "4": 10000, "5": 1000, "6": 2000, "6v": 2000, "7": 5000,
                  "8": 10000, "9": 20000}
 METRIC = "indexer key-positions scored/s & achieved HBM GB/s (frac of roofline), 1 GB300"
 
@@ -252,7 +254,12 @@ class DeviceCall:
         self.q = torch.from_numpy(w.q_bits.view(np.int16)).to(device)
         self.wt = torch.from_numpy(w.w).to(device)
         self.kcache = torch.from_numpy(w.kcache).to(device)
-        self.bt = torch.from_numpy(w.block_table).to(device)
+        self.cu_q = None
+        if w.meta.get("varlen"):              # one table row per request, and the offsets
+            self.cu_q, self.req_table = wl.request_tables(w)
+            self.bt = torch.from_numpy(self.req_table).to(device)
+        else:
+            self.bt = torch.from_numpy(w.block_table).to(device)
         self.seqlens = torch.from_numpy(w.seqlens).to(device)
         if w.kind == "topk":
             k = w.meta["k_top"]
@@ -265,6 +272,18 @@ class DeviceCall:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.kscale = (None if w.kscale_offset is None
                        else self.kcache.data_ptr() + w.kscale_offset)
+
+    def host_table(self):
+        """The block table this call copies in: per request or per row."""
+        return self.req_table if self.cu_q is not None else self.w.block_table
+
+    def launches(self):
+        """Kernels one call launches."""
+        if self.w.kind == "topk":
+            return 2
+        if self.cu_q is not None:
+            return sum(1 for a, b in zip(self.cu_q, self.cu_q[1:]) if b > a)
+        return 1
 
     def nbytes(self):
         if self.w.kind == "store":
@@ -305,6 +324,17 @@ class DeviceCall:
             if out is not None and out is not self.idx:     # e2e: both results to one buffer
                 out[:, :k].copy_(self.idx.view(torch.float32))
                 out[:, k:].copy_(self.val)
+            return
+        if self.cu_q is not None:
+            out = self.out if out is None else out
+            st = lib.dsa_indexer_logits_prefill_varlen(
+                self.q if q is None else q, self.wt if wt is None else wt, self.kcache,
+                self.kscale, w.page_stride, w.num_pages, w.kv_dtype,
+                self.bt if bt is None else bt, w.W, self.cu_q,
+                self.seqlens if seqlens is None else seqlens, w.H, w.D, w.P, w.W, out,
+                out.stride(0), self.status, torch.cuda.current_stream().cuda_stream)
+            if st != 0:
+                raise RuntimeError(f"library call failed: {lib.dsa_status_string(st)}")
             return
         if self._fn is None:
             self._fn = (lib.dsa_indexer_logits_decode if w.kind == "decode"
@@ -479,9 +509,10 @@ def run_ours(args, rank, world, local_rank):
         "gb_per_s": K * step_bytes / (elapsed_ms / 1e3) / 1e9,
         "roofline": roof,
         "clocks": sampler.summary(t_wall0, t_wall1),
-        # a top-k call is two kernels (logits, then the selection)
-        "gpu_launches": K * sum(2 if w.kind == "topk" else 1 for w in works),
-        "gpu_launches_kernel_region": dom_launches * (2 if dom.kind == "topk" else 1),
+        # a top-k call is two kernels (logits, then the selection); a varlen
+        # prefill call one per request
+        "gpu_launches": K * sum(c.launches() for c in copies[0]),
+        "gpu_launches_kernel_region": dom_launches * copies[0][dom_idx].launches(),
     }
 
     if not args.no_e2e:
@@ -513,7 +544,7 @@ def run_e2e(works, device, n_steps):
     host_parts = []
     for c in calls:
         host_parts += [torch.from_numpy(c.w.q_bits.view(np.int16)), torch.from_numpy(c.w.w),
-                       torch.from_numpy(c.w.block_table), torch.from_numpy(c.w.seqlens)]
+                       torch.from_numpy(c.host_table()), torch.from_numpy(c.w.seqlens)]
     in_offs, in_total = pack(host_parts)
     h_in = torch.empty(in_total, dtype=torch.uint8).pin_memory()
     d_in = torch.empty(in_total, dtype=torch.uint8, device=device)

@@ -146,6 +146,35 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
                                float* out, long long out_stride,
                                int* dev_status, void* stream);
 
+/*
+ * Prefill of several requests in one call, with a table row per request:
+ * the query tokens of request b are rows [cu_q[b], cu_q[b+1]) of q, w,
+ * seqlens and out, and read the keys through block-table row b
+ * (block_table + b * bt_stride; bt_stride >= W, or 0 for one row shared by
+ * all requests).  Query i may see the positions t < seqlens[i] (its causal
+ * limit + 1), as in dsa_indexer_logits_prefill; positions past it hold
+ * -inf.  No gathered per-query copy of the keys is made ("The Dispatch
+ * Decision ...", section "The Problem That Led Here": the materialised
+ * [query tokens, pages, ...] gather is what ran out of memory).
+ *
+ * cu_q is a HOST array of n_req + 1 offsets: cu_q[0] = 0, non-decreasing
+ * (DSA_ERR_INVALID_ARG otherwise, checked before any launch); n_q =
+ * cu_q[n_req] rows in all.  Each non-empty request runs the query-tile
+ * kernel of dsa_indexer_logits_prefill (one launch each, in request order,
+ * on `stream`), so requests of many tokens reuse each key tile four times;
+ * requests of one or a few tokens are better served by per-query rows.
+ * Other arguments, layouts, alignment, range and device errors as for
+ * dsa_indexer_logits_prefill.  DSA_ERR_CUDA from a launch may leave the
+ * earlier requests launched.
+ */
+int dsa_indexer_logits_prefill_varlen(const void* q, const float* w, const void* kcache,
+                                      const void* kscale, long long page_stride_bytes,
+                                      int num_pages, int kv_dtype, const int* block_table,
+                                      long long bt_stride, const int* cu_q, int n_req,
+                                      const int* seqlens, int H, int D, int page_size, int W,
+                                      float* out, long long out_stride, int* dev_status,
+                                      void* stream);
+
 /* A static, human-readable name for a status code. */
 /*
  * Decode with top-k selection: for every request b, the k_top positions

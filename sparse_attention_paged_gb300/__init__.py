@@ -12,6 +12,8 @@ For each row r and position t < W*64:
 """
 from __future__ import annotations
 
+import ctypes
+
 from . import _native
 
 KV_FP8_E4M3 = 0
@@ -82,6 +84,23 @@ def dsa_indexer_logits_prefill(q, w, kcache, kscale, page_stride_bytes, num_page
         _p(q), _p(w), _p(kcache), _p(kscale), int(page_stride_bytes), int(num_pages),
         int(kv_dtype), _p(block_table), int(bt_stride), _p(seqlens), int(n_q), int(H),
         int(D), int(page_size), int(W), _p(out), int(out_stride), _p(dev_status),
+        _stream(stream)))
+
+
+def dsa_indexer_logits_prefill_varlen(q, w, kcache, kscale, page_stride_bytes, num_pages,
+                                      kv_dtype, block_table, bt_stride, cu_q, seqlens, H, D,
+                                      page_size, W, out, out_stride, dev_status=None,
+                                      stream=None) -> int:
+    """C ``dsa_indexer_logits_prefill_varlen``; returns its status code.  `cu_q`
+    is host data (a sequence of n_req + 1 ints); n_req = len(cu_q) - 1."""
+    offs = [int(v) for v in cu_q]
+    n_req = max(len(offs) - 1, 0)
+    arr = (ctypes.c_int * max(len(offs), 1))(*offs)
+    return int(_native.load().dsa_indexer_logits_prefill_varlen(
+        _p(q), _p(w), _p(kcache), _p(kscale), int(page_stride_bytes), int(num_pages),
+        int(kv_dtype), _p(block_table), int(bt_stride),
+        ctypes.cast(arr, ctypes.c_void_p).value if offs else None, n_req, _p(seqlens),
+        int(H), int(D), int(page_size), int(W), _p(out), int(out_stride), _p(dev_status),
         _stream(stream)))
 
 

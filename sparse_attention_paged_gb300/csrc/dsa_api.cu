@@ -123,6 +123,43 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
+int dsa_indexer_logits_prefill_varlen(const void* q, const float* w, const void* kcache,
+                                      const void* kscale, long long page_stride_bytes,
+                                      int num_pages, int kv_dtype, const int* block_table,
+                                      long long bt_stride, const int* cu_q, int n_req,
+                                      const int* seqlens, int H, int D, int page_size, int W,
+                                      float* out, long long out_stride, int* dev_status,
+                                      void* stream) {
+  // the request boundaries are host data: checked here, before any launch
+  if (n_req < 0 || (n_req > 0 && cu_q == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (n_req > 0 && cu_q[0] != 0) return DSA_ERR_INVALID_ARG;
+  for (int b = 0; b < n_req; ++b)
+    if (cu_q[b + 1] < cu_q[b]) return DSA_ERR_INVALID_ARG;
+  const int n_q = n_req > 0 ? cu_q[n_req] : 0;
+  dsa::RowsParams p;
+  int st = check_and_pack(q, w, kcache, kscale, page_stride_bytes, num_pages, kv_dtype,
+                          block_table, bt_stride, seqlens, n_q, H, D, page_size, W, out,
+                          out_stride, dev_status, &p);
+  if (st != DSA_OK) return st;
+  // one query-tile launch per request: its queries, lengths and output rows,
+  // over its own table row
+  for (int b = 0; b < n_req; ++b) {
+    const int a = cu_q[b], n = cu_q[b + 1] - cu_q[b];
+    if (n == 0) continue;
+    dsa::RowsParams pb = p;
+    pb.q = p.q + (long long)a * dsa::kHeads * dsa::kDim;
+    pb.w = p.w + (long long)a * dsa::kHeads;
+    pb.seqlens = p.seqlens + a;
+    pb.out = p.out + (long long)a * p.out_stride;
+    pb.block_table = p.block_table + (long long)b * bt_stride;
+    pb.bt_stride = 0;
+    pb.rows = n;
+    if (dsa::launch_prefill(pb, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
+}
+
 int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
                             const void* kscale, long long page_stride_bytes, int num_pages,
                             int kv_dtype, const int* block_table, long long bt_stride,

@@ -274,6 +274,23 @@ def prefill_varlen(name: str, requests, seed: int = 0, kv_dtype: int = KV_BF16) 
                      meta={"requests": reqs, "groups": groups})
 
 
+def request_tables(w: Workload):
+    """The request offsets (cu_q, host ints) and one block-table row per
+    request of a several-request prefill workload (its per-query rows are
+    copies of their request's row)."""
+    groups = w.meta["groups"]
+    cu = [0]
+    for _, n in groups:
+        cu.append(cu[-1] + n)
+    rows = []
+    for b, (a, n) in enumerate(groups):
+        if n > 0:
+            rows.append(w.block_table[a])
+        else:                                   # no query token carries its row: any valid row
+            rows.append(np.full(w.W, w.num_pages - 1, dtype=w.block_table.dtype))
+    return cu, np.stack(rows)
+
+
 # ---------------------------------------------------------------------------
 # The named workloads.
 
@@ -408,6 +425,15 @@ def cfg6() -> Workload:
                           [(256, 6144), (512, 12288), (128, 3072), (1024, 20480)], seed=0)
 
 
+def cfg6v() -> Workload:
+    """Config 6's four requests called with one block-table row per request
+    and the request offsets: one query-tile launch per request."""
+    w = cfg6()
+    w.name = "prefill_bf16_varlen4_q1920_reqrows"
+    w.meta["varlen"] = True
+    return w
+
+
 def cfg7() -> Workload:
     """Prefill with fp8 keys: 1,024 query tokens of one request over 128
     pages (8,192 positions), causal limit of query i = 7168 + i."""
@@ -424,6 +450,7 @@ NAMED = {
     "4": lambda: [cfg4()],
     "5": lambda: [cfg5()],
     "6": lambda: [cfg6()],
+    "6v": lambda: [cfg6v()],
     "7": lambda: [cfg7()],
     "8": lambda: [cfg8()],
     "9": lambda: [cfg9()],

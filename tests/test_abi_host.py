@@ -145,3 +145,34 @@ def test_topk_rejects_bad_arguments(lib, kw, code):
 @needs_nvcc
 def test_topk_zero_rows_is_a_no_op(lib):
     assert topk_call(B=0) == 0
+
+
+def call_varlen(**kw):
+    import sparse_attention_paged_gb300 as s
+    args = dict(q=A, w=A, kcache=A, kscale=A + 8192, page_stride_bytes=8448, num_pages=16,
+                kv_dtype=0, block_table=A, bt_stride=8, cu_q=[0, 3, 5], seqlens=A, H=64,
+                D=128, page_size=64, W=8, out=A, out_stride=512, dev_status=None, stream=0)
+    args.update(kw)
+    return s.dsa_indexer_logits_prefill_varlen(**args)
+
+
+@needs_nvcc
+@pytest.mark.parametrize("kw, code", [
+    (dict(cu_q=[1, 3, 5]), 1),                 # offsets must start at 0
+    (dict(cu_q=[0, 5, 3]), 1),                 # and not decrease
+    (dict(bt_stride=4), 1),                    # a table row per request: bt_stride >= W
+    (dict(q=None), 1),
+    (dict(H=32), 2),
+    (dict(out_stride=256), 1),
+    (dict(q=A + 8), 3),
+])
+def test_prefill_varlen_rejects_bad_arguments(lib, kw, code):
+    assert call_varlen(**kw) == code
+
+
+@needs_nvcc
+def test_prefill_varlen_without_query_tokens_is_a_no_op(lib):
+    # no rows: nothing is launched, whatever the (fake) pointers
+    assert call_varlen(cu_q=[]) == 0
+    assert call_varlen(cu_q=[0]) == 0
+    assert call_varlen(cu_q=[0, 0, 0]) == 0
