@@ -245,6 +245,7 @@ class DeviceCall:
         import torch
         self.w = w
         self._fn = None
+        self.cu_q = None                       # request offsets of a varlen prefill call
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         if w.kind == "store":
             self.k = torch.from_numpy(w.k_bits.view(np.int16)).to(device)
@@ -254,7 +255,6 @@ class DeviceCall:
         self.q = torch.from_numpy(w.q_bits.view(np.int16)).to(device)
         self.wt = torch.from_numpy(w.w).to(device)
         self.kcache = torch.from_numpy(w.kcache).to(device)
-        self.cu_q = None
         if w.meta.get("varlen"):              # one table row per request, and the offsets
             self.cu_q, self.req_table = wl.request_tables(w)
             self.bt = torch.from_numpy(self.req_table).to(device)
@@ -524,6 +524,39 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def _time_e2e_steps(step, n_steps):
+    """Time n_steps end-to-end steps two ways: eagerly (every call issued
+    from Python) and as replays of a CUDA graph of up to 100 steps (the
+    library calls are capturable); every step, either way, copies its own
+    inputs in and its results out.  Returns (graph ms, eager ms, steps)."""
+    import torch
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1)
+    G = min(100, n_steps)
+    reps = max(1, n_steps // G)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(G):
+            step()
+    g.replay()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), eager_ms, reps * G, G
+
+
 def run_e2e(works, device, n_steps):
     """The same metric through the public API with host buffers: every step
     copies its inputs (q, w, block tables, lengths of every call, packed in
@@ -567,21 +600,15 @@ def run_e2e(works, device, n_steps):
             q, wt, bt, sl = views[4 * j: 4 * j + 4]
             c(q=q, wt=wt, bt=bt, seqlens=sl, out=outs[j])
         h_out.copy_(d_out, non_blocking=True)
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(n_steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms, eager_ms, steps, G = _time_e2e_steps(step, n_steps)
     pos = sum(w.valid_positions for w in works)
-    return {"value": n_steps * pos / (ms / 1e3), "unit": "key-positions/s",
-            "steps": n_steps, "ms_per_step": ms / n_steps,
-            "h2d_bytes_per_step": in_total, "d2h_bytes_per_step": out_total}
+    return {"value": steps * pos / (ms / 1e3), "unit": "key-positions/s",
+            "steps": steps, "ms_per_step": ms / steps,
+            "h2d_bytes_per_step": in_total, "d2h_bytes_per_step": out_total,
+            "timing": f"CUDA graphs of {G} steps (each: one H2D copy of the step's inputs "
+                      "from pinned memory, the calls, one D2H copy of the results)",
+            "eager_value": n_steps * pos / (eager_ms / 1e3),
+            "eager_ms_per_step": eager_ms / n_steps}
 
 
 def run_e2e_store(works, device, n_steps):
@@ -602,22 +629,16 @@ def run_e2e_store(works, device, n_steps):
             d_s[j].copy_(h_s[j], non_blocking=True)
             c.store(k=d_k[j], slots=d_s[j])
             h_st[j:j + 1].copy_(c.status, non_blocking=True)
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(n_steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms, eager_ms, steps, G = _time_e2e_steps(step, n_steps)
     rows = sum(w.valid_positions for w in works)
-    return {"value": n_steps * rows / (ms / 1e3), "unit": "key-positions/s",
-            "steps": n_steps, "ms_per_step": ms / n_steps,
+    return {"value": steps * rows / (ms / 1e3), "unit": "key-positions/s",
+            "steps": steps, "ms_per_step": ms / steps,
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_k + h_s),
-            "d2h_bytes_per_step": 4 * len(calls)}
+            "d2h_bytes_per_step": 4 * len(calls),
+            "timing": f"CUDA graphs of {G} steps (each: H2D copies of the step's rows and "
+                      "slots from pinned memory, the store, D2H copy of the status)",
+            "eager_value": n_steps * rows / (eager_ms / 1e3),
+            "eager_ms_per_step": eager_ms / n_steps}
 
 
 # ---------------------------------------------------------------------------
