@@ -20,6 +20,7 @@
 // conflicts and in-order output offsets come from warp ballots.  Rows of at
 // most k valid positions take all of them; the rest of the k outputs is -1
 // (value -inf).
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -29,6 +30,8 @@
 #include "sm100_ptx.cuh"
 
 namespace dsa {
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -92,13 +95,18 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* ws, int& total) 
 // Finds the bin holding the need-th largest entry of hist[0, nbins) counted
 // from the top (nbins <= 2 * kTkThreads): every thread takes two bins, a
 // block scan from the top gives each its count above; returns the bin and
-// writes the count above it to *above and its own count to *pop.
-__device__ __forceinline__ int find_bin(const uint32_t* hist, int nbins, int need, int* ws,
-                                        int* sh_pick, int* above, int* pop) {
+// writes the count above it to *above and its own count to *pop.  hist2,
+// when given, is added bin by bin (the other half of a row).
+__device__ __forceinline__ int find_bin(const uint32_t* hist, const uint32_t* hist2, int nbins,
+                                        int need, int* ws, int* sh_pick, int* above, int* pop) {
   const int t = threadIdx.x;
   const int b1 = nbins - 1 - 2 * t, b0 = b1 - 1;             // this thread's bins, high first
-  const int h1 = b1 >= 0 ? (int)hist[b1] : 0;
-  const int h0 = b0 >= 0 ? (int)hist[b0] : 0;
+  int h1 = b1 >= 0 ? (int)hist[b1] : 0;
+  int h0 = b0 >= 0 ? (int)hist[b0] : 0;
+  if (hist2 != nullptr) {
+    h1 += b1 >= 0 ? (int)hist2[b1] : 0;
+    h0 += b0 >= 0 ? (int)hist2[b0] : 0;
+  }
   int total;
   const int before = block_exclusive_scan(h1 + h0, ws, total);   // entries in higher bins
   if (before < need && before + h1 >= need) {
@@ -135,9 +143,13 @@ __device__ __forceinline__ int warp_sum(int v) {
   return v;
 }
 
+// kCl CTAs per row (1, or a cluster of 2 that splits the row in halves and
+// exchanges its range, histogram, collected keys and counts through
+// distributed shared memory).
+template <int kCl>
 __global__ void __launch_bounds__(kTkThreads)
     topk_kernel(const TopkParams p) {
-  extern __shared__ __align__(16) float row_s[];             // the row, when it fits
+  extern __shared__ __align__(16) float row_s[];             // the CTA's part of the row, when it fits
   __shared__ __align__(16) uint32_t hist[2048];
   __shared__ uint32_t cand_key[kCand];
   __shared__ int cand_pos[kCand];
@@ -146,7 +158,10 @@ __global__ void __launch_bounds__(kTkThreads)
   __shared__ float red[2][kTkWarps];
   __shared__ int w_gt[kTkWarps], w_eq[kTkWarps], w_out[kTkWarps], w_take[kTkWarps];
   __shared__ int n_cand;
-  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ float part_range[kCl][2];       // each CTA's sample (min, max)
+  __shared__ int part_def, taken_first;      // positions in bins above lb; collected ones taken in part 0
+  const int r = blockIdx.x / kCl, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int crank = kCl > 1 ? (int)cg::this_cluster().block_rank() : 0;
   // the logits were written by the previous launch
   sm100::griddep_wait();
   sm100::griddep_launch_dependents();
@@ -157,24 +172,30 @@ __global__ void __launch_bounds__(kTkThreads)
   int* orow = p.idx + (long long)r * p.out_stride;
   float* vrow = p.vals ? p.vals + (long long)r * p.out_stride : nullptr;
   if (bad && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
-  if (L <= p.k) {
-    for (int j = tid; j < p.k; j += kTkThreads) {
-      orow[j] = j < L ? j : -1;
-      if (vrow) vrow[j] = j < L ? grow[j] : -INFINITY;
+  if (L <= p.k) {                            // the whole cluster takes this branch
+    if (crank == 0) {
+      for (int j = tid; j < p.k; j += kTkThreads) {
+        orow[j] = j < L ? j : -1;
+        if (vrow) vrow[j] = j < L ? grow[j] : -INFINITY;
+      }
     }
     return;
   }
 
-  // Warp w owns float4s [w_beg, w_end) of the row; the last float4 may run
-  // past L (still inside the row's T >= L floats, or the shared cache, both
-  // multiples of 4), and its positions >= L are masked everywhere.
+  // The CTA owns float4s [cb4, cb4 + cn4) of the row (its part) and warp w
+  // of it float4s [w_beg, w_end); the last float4 may run past L (still
+  // inside the row's T >= L floats, or the shared cache, both multiples of
+  // 4), and its positions >= L are masked everywhere.  Segments are sized
+  // from the largest part, so every CTA of a cluster has the same steps.
   const int n4 = (L + 3) >> 2;
-  const int seg4 = (n4 + kTkWarps - 1) / kTkWarps;
-  const int w_beg = min(n4, warp * seg4), w_end = min(n4, w_beg + seg4);
-  const bool cached = 4 * n4 <= p.cache_floats;
+  const int p4 = (n4 + kCl - 1) / kCl;
+  int cb4 = min(n4, crank * p4), cn4 = min(n4, cb4 + p4) - cb4;
+  int seg4 = (p4 + kTkWarps - 1) / kTkWarps;
+  int w_beg = cb4 + min(cn4, warp * seg4), w_end = cb4 + min(cn4, warp * seg4 + seg4);
+  bool cached = 4 * cn4 <= p.cache_floats;
   float4* s4 = reinterpret_cast<float4*>(row_s);
   const float4* g4 = reinterpret_cast<const float4*>(grow);    // rows are 256-byte aligned
-  auto ld4 = [&](int j) -> float4 { return cached ? s4[j] : __ldcg(g4 + j); };
+  auto ld4 = [&](int j) -> float4 { return cached ? s4[j - cb4] : __ldcg(g4 + j); };
   // valid positions in float4 j (0 past the warp's segment)
   auto nvalid = [&](int j) { return j < w_end ? min(4, L - 4 * j) : 0; };
   // every float4 of the warp's segment, four 16-byte loads in flight; fn runs
@@ -237,6 +258,24 @@ __global__ void __launch_bounds__(kTkThreads)
     mn = fminf(mn, red[0][w8]);
     mx = fmaxf(mx, red[1][w8]);
   }
+  if constexpr (kCl > 1) {                   // the cluster's range: every part's sample
+    cg::cluster_group cluster = cg::this_cluster();
+    if (tid == 0) {
+      for (int c = 0; c < kCl; ++c) {
+        float* pr = cluster.map_shared_rank(&part_range[0][0], c);
+        pr[2 * crank] = mn;
+        pr[2 * crank + 1] = mx;
+      }
+      part_def = 0;
+      taken_first = 0;
+    }
+    cluster.sync();
+#pragma unroll
+    for (int c = 0; c < kCl; ++c) {
+      mn = fminf(mn, part_range[c][0]);
+      mx = fmaxf(mx, part_range[c][1]);
+    }
+  }
   float span = mx - mn, lo = mn;
   if (span > 0.f && span < INFINITY) {
     lo = mn - 0.125f * span;
@@ -251,12 +290,12 @@ __global__ void __launch_bounds__(kTkThreads)
   // ---- one pass over the row: into shared memory (if it fits), the
   // histogram, and each position's bin (16 bits, when the row and its bins
   // fit)
-  const bool bins_cached = 6 * n4 <= p.cache_floats;
-  uint2* b2 = reinterpret_cast<uint2*>(row_s + 4 * n4);       // four bins per float4
+  bool bins_cached = 6 * cn4 <= p.cache_floats;
+  uint2* b2 = reinterpret_cast<uint2*>(row_s + 4 * cn4);      // four bins per float4
   auto bin_float4 = [&](int j, float4 v) {
     const int nv = nvalid(j);
     if (nv == 0) return;
-    if (cached) s4[j] = v;
+    if (cached) s4[j - cb4] = v;
     const float x[4] = {v.x, v.y, v.z, v.w};
     uint32_t bq[4];
 #pragma unroll
@@ -264,7 +303,7 @@ __global__ void __launch_bounds__(kTkThreads)
       bq[e] = (uint32_t)lbin(x[e]);
       if (e < nv) atomicAdd(&hist[bq[e]], 1u);
     }
-    if (bins_cached) b2[j] = make_uint2(bq[0] | (bq[1] << 16), bq[2] | (bq[3] << 16));
+    if (bins_cached) b2[j - cb4] = make_uint2(bq[0] | (bq[1] << 16), bq[2] | (bq[3] << 16));
   };
   bin_float4(j_first, v_first);
   for (int j0 = w_beg + 32; j0 < w_end; j0 += 8 * 32) {      // eight 16-byte loads in flight
@@ -280,8 +319,15 @@ __global__ void __launch_bounds__(kTkThreads)
   __syncthreads();
   int need = p.k;                            // entries still to take at or below the prefix
   int above, pop;
-  const int lb = find_bin(hist, 2048, need, ws, sh_pick, &above, &pop);
+  const uint32_t* hist_peer = nullptr;
+  if constexpr (kCl > 1) {                   // both halves' histograms complete
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    hist_peer = cluster.map_shared_rank(hist, 1 - crank);
+  }
+  const int lb = find_bin(hist, hist_peer, 2048, need, ws, sh_pick, &above, &pop);
   need -= above;
+  if constexpr (kCl > 1) cg::this_cluster().sync();   // no CTA reads the other's histogram now
 
   // ---- the k-th largest key K* among the members of bin lb: the collected
   // keys, or the whole row by radix passes when the bin holds more than
@@ -296,6 +342,18 @@ __global__ void __launch_bounds__(kTkThreads)
   const bool collect = pop <= kCand;
   const int S = (seg4 + 31) >> 5;            // steps of 32 float4s in a warp's segment
   const bool fast = pop <= kRankMax && S <= kMaskSteps;
+  if (kCl > 1 && !fast) {
+    // the general path runs on the cluster's first CTA alone, over the
+    // whole row, read from global memory
+    if (crank != 0) return;
+    cb4 = 0;
+    cn4 = n4;
+    seg4 = (n4 + kTkWarps - 1) / kTkWarps;
+    w_beg = min(n4, warp * seg4);
+    w_end = min(n4, w_beg + seg4);
+    cached = false;
+    bins_cached = false;
+  }
   uint32_t* tmask = hist;
   auto mask_word = [&](int w, int step, int e) -> uint32_t& {
     return tmask[(w * kMaskSteps + step) * 4 + e];
@@ -353,7 +411,7 @@ __global__ void __launch_bounds__(kTkThreads)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int j = j0 + u * 32 + lane;
-        bb[u] = j < w_end ? b2[j] : make_uint2(0u, 0u);
+        bb[u] = j < w_end ? b2[j - cb4] : make_uint2(0u, 0u);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -365,7 +423,7 @@ __global__ void __launch_bounds__(kTkThreads)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           if (e >= nv) b[e] = -1;
-        collect_step(j, b, [&] { return s4[j]; });
+        collect_step(j, b, [&] { return s4[j - cb4]; });
       }
     }
   } else if (collect) {
@@ -378,10 +436,31 @@ __global__ void __launch_bounds__(kTkThreads)
       collect_step(j, b, [&] { return v; });
     });
   }
-  const int nc = min(pop, kCand);
-  auto warp_of = [&](int pos) { return (pos >> 2) / seg4; };
+  int nc = min(pop, kCand);
+  auto warp_of = [&](int pos) { return ((pos >> 2) - cb4) / seg4; };
   uint32_t kstar = 0;
+  int part_base = 0;                         // outputs of the parts before this CTA's
   if (fast) {
+    if constexpr (kCl > 1) {
+      // the other half's collected keys join this CTA's (after its own),
+      // with its count of positions in bins above lb
+      cg::cluster_group cluster = cg::this_cluster();
+      const int g = warp_sum(n_gt_bins);
+      if (lane == 0) atomicAdd(&part_def, g);
+      cluster.sync();                        // both halves collected
+      const int other = 1 - crank;
+      const int n_own = n_cand;
+      const int n_other = *cluster.map_shared_rank(&n_cand, other);
+      const uint32_t* other_key = cluster.map_shared_rank(cand_key, other);
+      const int* other_pos = cluster.map_shared_rank(cand_pos, other);
+      for (int i = tid; i < n_other; i += kTkThreads) {
+        cand_key[n_own + i] = other_key[i];
+        cand_pos[n_own + i] = other_pos[i];
+      }
+      if (crank == 1) part_base = *cluster.map_shared_rank(&part_def, other);
+      nc = n_own + n_other;
+      cluster.sync();                        // no CTA reads the other's shared memory after this
+    }
     // thread i ranks collected key i: the keys above it, equal to it, and
     // equal to it at a lower position; every thread holding a copy of the
     // need-th largest writes the same pair
@@ -407,10 +486,16 @@ __global__ void __launch_bounds__(kTkThreads)
     kstar = (uint32_t)sh_pick[0];
     need -= sh_pick[1];                      // copies of K* taken, lowest positions first
     if (tid < nc && (key > kstar || (key == kstar && eq_lower < need))) {
-      const int j = pos >> 2, w = warp_of(pos), rel = j - w * seg4;
-      atomicOr(&mask_word(w, rel >> 5, pos & 3), 1u << (rel & 31));
+      const int j = pos >> 2;
+      if (j >= cb4 && j < cb4 + cn4) {         // this CTA's part: into its masks
+        const int w = warp_of(pos), rel = j - cb4 - w * seg4;
+        atomicOr(&mask_word(w, rel >> 5, pos & 3), 1u << (rel & 31));
+      } else if (j < cb4) {                    // the first part's: its outputs come first
+        atomicAdd(&taken_first, 1);
+      }
     }
     __syncthreads();
+    if (kCl > 1 && crank == 1) part_base += taken_first;
     int cnt = 0;
     for (int i = lane; i < S * 4; i += 32) cnt += __popc(tmask[warp * kMaskSteps * 4 + i]);
     cnt = warp_sum(cnt);
@@ -446,7 +531,7 @@ __global__ void __launch_bounds__(kTkThreads)
         });
       }
       __syncthreads();
-      const int bin = find_bin(hist, nbins, need, ws, sh_pick, &above, &pop);
+      const int bin = find_bin(hist, nullptr, nbins, need, ws, sh_pick, &above, &pop);
       prefix |= (uint32_t)bin << shift;
       mask |= (uint32_t)(nbins - 1) << shift;
       need -= above;
@@ -504,7 +589,7 @@ __global__ void __launch_bounds__(kTkThreads)
       const int y = __shfl_up_sync(0xffffffffu, ts, o);
       if (lane >= o) ts += y;
     }
-    w_out[lane] = ts - (g + take);
+    w_out[lane] = part_base + ts - (g + take);
     w_take[lane] = take;
   }
   __syncthreads();
@@ -601,36 +686,51 @@ cudaError_t launch_topk(const float* logits, long long ld, const int* seqlens, i
                         int k, int* idx, float* vals, long long out_stride, int* status,
                         cudaStream_t stream) {
   // shared memory for the row cache: the per-block opt-in less the static
-  // arrays, set once per device
+  // arrays; and the SM count.  Set once per device.
   static int cache_per_dev[kMaxDevices] = {0};
+  static int sms_per_dev[kMaxDevices] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (cache_per_dev[dev] == 0) {
-    int optin = 0;
+    int optin = 0, sms = 0;
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
         cudaSuccess)
       return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
     const int bytes = ((optin - kStaticSmemReserve) / 16) * 16;   // room for the static arrays
-    if ((e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(topk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   bytes)) != cudaSuccess)
       return e;
+    if ((e = cudaFuncSetAttribute(topk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  bytes)) != cudaSuccess)
+      return e;
+    sms_per_dev[dev] = sms;
     cache_per_dev[dev] = bytes;
   }
   const int bytes = cache_per_dev[dev];
   const TopkParams p{logits, ld, seqlens, rows, T, k, idx, vals, out_stride, status, bytes / 4};
+  // two CTAs per row (one cluster each) while they all fit in one wave of
+  // one CTA per SM; else one CTA per row
+  const bool pairs = 2ll * rows <= sms_per_dev[dev];
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(rows);
+  cfg.gridDim = dim3(pairs ? 2 * rows : rows);
   cfg.blockDim = dim3(kTkThreads);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = pairs ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_kernel, p);
+  cfg.numAttrs = pairs ? 2 : 1;
+  return pairs ? cudaLaunchKernelEx(&cfg, topk_kernel<2>, p)
+               : cudaLaunchKernelEx(&cfg, topk_kernel<1>, p);
 }
 
 }  // namespace dsa

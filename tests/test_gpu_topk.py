@@ -145,3 +145,17 @@ def test_topk_rows_longer_than_the_shared_cache():
         idx, val, st = _topk(w, k)
         assert st == 0
         _check(w, k, idx, val, list(range(w.R)))
+
+
+@pytest.mark.parametrize("k", [64, 300])
+def test_topk_more_rows_than_pairs_of_sms(k):
+    """More than half as many rows as SMs: one CTA per row instead of a
+    cluster of two."""
+    W = 20
+    g = np.random.default_rng(5)
+    lens = [int(x) for x in g.integers(0, W * 64 + 1, 100)]
+    lens[:4] = [0, k, k + 1, W * 64]
+    w = wl.decode_with_lengths(f"tk_many{k}", lens, W, seed=33)
+    idx, val, st = _topk(w, k)
+    assert st == 0
+    _check(w, k, idx, val, list(range(w.R)))
