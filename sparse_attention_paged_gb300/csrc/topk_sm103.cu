@@ -41,8 +41,9 @@ static_assert(kTkWarps == 32, "the per-warp scans run on one warp's lanes");
 constexpr int kCand = 2048;                  // keys of the k-th largest's bin kept for the exact passes
 constexpr int kRankMax = 128;                // at most this many collected keys: ranked directly
 constexpr int kMaskSteps = 16;               // steps of 32 float4s per warp kept as vote masks
-static_assert(kTkWarps * kMaskSteps * 4 == 2048, "the vote masks take the histogram's place");
-constexpr int kStaticSmemReserve = 28 * 1024;  // the kernel's static shared arrays fit in this
+static_assert(kTkWarps * kMaskSteps * 4 == 2048, "one mask word per warp, step and element");
+static_assert(2 * kRankMax <= kCand / 2, "a pair's collected keys fit in half of the buffer");
+constexpr int kStaticSmemReserve = 36 * 1024;  // the kernel's static shared arrays fit in this
 
 struct TopkParams {
   const float* logits;   // row r at logits + r * ld, positions [0, L_r) valid
@@ -158,8 +159,11 @@ __global__ void __launch_bounds__(kTkThreads)
   __shared__ float red[2][kTkWarps];
   __shared__ int w_gt[kTkWarps], w_eq[kTkWarps], w_out[kTkWarps], w_take[kTkWarps];
   __shared__ int n_cand;
-  __shared__ float part_range[kCl][2];       // each CTA's sample (min, max)
-  __shared__ int part_def, taken_first;      // positions in bins above lb; collected ones taken in part 0
+  __shared__ __align__(16) uint32_t tmask[2048];               // vote masks of the positions taken
+  // a pair's exchange: the other CTA's collected count and count of
+  // positions in bins above lb (written by it), this CTA's count, and the
+  // collected positions of the first half that are taken
+  __shared__ int peer_n, peer_def, own_def, taken_first;
   const int r = blockIdx.x / kCl, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int crank = kCl > 1 ? (int)cg::this_cluster().block_rank() : 0;
   // the logits were written by the previous launch
@@ -239,6 +243,24 @@ __global__ void __launch_bounds__(kTkThreads)
       }
     }
   }
+  if constexpr (kCl > 1) {
+    // the other half's sample too, read from global memory, so that both
+    // CTAs of the pair bin over the same range without an exchange
+    const int o_cb4 = min(n4, (1 - crank) * p4), o_cn4 = min(n4, o_cb4 + p4) - o_cb4;
+    const int jo = o_cb4 + min(o_cn4, warp * seg4) + lane;
+    if (jo < o_cb4 + min(o_cn4, warp * seg4 + seg4)) {
+      const float4 v = __ldcg(g4 + jo);
+      const float x[4] = {v.x, v.y, v.z, v.w};
+      const int nv = min(4, L - 4 * jo);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (e < nv) {
+          mn = fminf(mn, x[e]);
+          mx = fmaxf(mx, x[e]);
+        }
+      }
+    }
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
@@ -249,7 +271,15 @@ __global__ void __launch_bounds__(kTkThreads)
     red[1][warp] = mx;
   }
   for (int b = tid; b < 2048; b += kTkThreads) hist[b] = 0;
-  if (tid == 0) n_cand = 0;
+  if (tid == 0) {
+    // (the other CTA of a pair writes peer_n / peer_def only after both
+    // have passed the histogram barrier, so these are cleared first)
+    n_cand = 0;
+    peer_n = 0;
+    peer_def = 0;
+    own_def = 0;
+    taken_first = 0;
+  }
   __syncthreads();
   mn = INFINITY;
   mx = -INFINITY;
@@ -257,24 +287,6 @@ __global__ void __launch_bounds__(kTkThreads)
   for (int w8 = 0; w8 < kTkWarps; ++w8) {
     mn = fminf(mn, red[0][w8]);
     mx = fmaxf(mx, red[1][w8]);
-  }
-  if constexpr (kCl > 1) {                   // the cluster's range: every part's sample
-    cg::cluster_group cluster = cg::this_cluster();
-    if (tid == 0) {
-      for (int c = 0; c < kCl; ++c) {
-        float* pr = cluster.map_shared_rank(&part_range[0][0], c);
-        pr[2 * crank] = mn;
-        pr[2 * crank + 1] = mx;
-      }
-      part_def = 0;
-      taken_first = 0;
-    }
-    cluster.sync();
-#pragma unroll
-    for (int c = 0; c < kCl; ++c) {
-      mn = fminf(mn, part_range[c][0]);
-      mx = fmaxf(mx, part_range[c][1]);
-    }
   }
   float span = mx - mn, lo = mn;
   if (span > 0.f && span < INFINITY) {
@@ -327,7 +339,6 @@ __global__ void __launch_bounds__(kTkThreads)
   }
   const int lb = find_bin(hist, hist_peer, 2048, need, ws, sh_pick, &above, &pop);
   need -= above;
-  if constexpr (kCl > 1) cg::this_cluster().sync();   // no CTA reads the other's histogram now
 
   // ---- the k-th largest key K* among the members of bin lb: the collected
   // keys, or the whole row by radix passes when the bin holds more than
@@ -344,7 +355,9 @@ __global__ void __launch_bounds__(kTkThreads)
   const bool fast = pop <= kRankMax && S <= kMaskSteps;
   if (kCl > 1 && !fast) {
     // the general path runs on the cluster's first CTA alone, over the
-    // whole row, read from global memory
+    // whole row, read from global memory (its histogram is reused once the
+    // other CTA has read it)
+    if constexpr (kCl > 1) cg::this_cluster().sync();
     if (crank != 0) return;
     cb4 = 0;
     cn4 = n4;
@@ -354,7 +367,6 @@ __global__ void __launch_bounds__(kTkThreads)
     cached = false;
     bins_cached = false;
   }
-  uint32_t* tmask = hist;
   auto mask_word = [&](int w, int step, int e) -> uint32_t& {
     return tmask[(w * kMaskSteps + step) * 4 + e];
   };
@@ -364,6 +376,14 @@ __global__ void __launch_bounds__(kTkThreads)
   }
   int n_gt_bins = 0;                         // this lane's positions in bins above lb
   const uint32_t lt = (1u << lane) - 1u;
+  uint32_t* peer_key = nullptr;              // a pair on the fast path: the other CTA's buffers
+  int* peer_pos = nullptr;
+  if constexpr (kCl > 1) {
+    if (fast) {
+      peer_key = cg::this_cluster().map_shared_rank(cand_key, 1 - crank);
+      peer_pos = cg::this_cluster().map_shared_rank(cand_pos, 1 - crank);
+    }
+  }
   // one step of the collection: b[e] is the bin of position 4j+e (-1 past
   // the segment); x_of() gives the float4, read only by lanes holding a
   // member of bin lb
@@ -401,6 +421,10 @@ __global__ void __launch_bounds__(kTkThreads)
         if (c[e] && i < kCand) {
           cand_key[i] = order_key(x[e]);
           cand_pos[i] = 4 * j + e;
+          if (peer_key != nullptr) {                      // a pair: the other CTA's copy
+            peer_key[kCand / 2 + i] = cand_key[i];
+            peer_pos[kCand / 2 + i] = cand_pos[i];
+          }
         }
       }
     }
@@ -442,24 +466,25 @@ __global__ void __launch_bounds__(kTkThreads)
   int part_base = 0;                         // outputs of the parts before this CTA's
   if (fast) {
     if constexpr (kCl > 1) {
-      // the other half's collected keys join this CTA's (after its own),
-      // with its count of positions in bins above lb
+      // each CTA has pushed its collected keys into the other's buffer (at
+      // kCand / 2); now its counts, then the pair's barrier: after it
+      // neither CTA touches the other's shared memory
       cg::cluster_group cluster = cg::this_cluster();
       const int g = warp_sum(n_gt_bins);
-      if (lane == 0) atomicAdd(&part_def, g);
-      cluster.sync();                        // both halves collected
-      const int other = 1 - crank;
-      const int n_own = n_cand;
-      const int n_other = *cluster.map_shared_rank(&n_cand, other);
-      const uint32_t* other_key = cluster.map_shared_rank(cand_key, other);
-      const int* other_pos = cluster.map_shared_rank(cand_pos, other);
-      for (int i = tid; i < n_other; i += kTkThreads) {
-        cand_key[n_own + i] = other_key[i];
-        cand_pos[n_own + i] = other_pos[i];
+      if (lane == 0) atomicAdd(&own_def, g);
+      __syncthreads();
+      if (tid == 0) {
+        *cluster.map_shared_rank(&peer_n, 1 - crank) = n_cand;
+        *cluster.map_shared_rank(&peer_def, 1 - crank) = own_def;
       }
-      if (crank == 1) part_base = *cluster.map_shared_rank(&part_def, other);
+      cluster.sync();                        // both halves collected and pushed
+      const int n_own = n_cand, n_other = peer_n;
+      for (int i = tid; i < n_other; i += kTkThreads) {   // the other half's keys after this one's
+        cand_key[n_own + i] = cand_key[kCand / 2 + i];
+        cand_pos[n_own + i] = cand_pos[kCand / 2 + i];
+      }
+      if (crank == 1) part_base = peer_def;
       nc = n_own + n_other;
-      cluster.sync();                        // no CTA reads the other's shared memory after this
     }
     // thread i ranks collected key i: the keys above it, equal to it, and
     // equal to it at a lower position; every thread holding a copy of the
