@@ -5,19 +5,22 @@
 // cached positions so that only the top-k enter attention); the selection
 // itself is a plain definition.
 //
-// One CTA per row.  Logits become order-preserving 32-bit keys (a larger
-// float gives a larger key; NaN, which only an error row holds, the smallest
-// key).  A histogram of 2,048 linear bins over the row's range finds the bin
-// of the k-th largest logit; one more pass over the row collects that bin's
-// members into shared memory (usually a handful) and counts, per warp, the
-// positions in higher bins; a three-pass radix select (11 + 11 + 10 bits)
-// over the collected keys then finds the k-th largest key K* and how many
-// keys equal to it are needed.  (A bin too full to collect is resolved by
-// the same radix passes over the whole row.)  A last pass writes, in
-// position order, every position whose key is above K* and the first needed
-// ones equal to it.  Each warp owns a contiguous segment of the row, its
-// lanes on consecutive float4s, so that shared-memory reads are free of bank
-// conflicts and in-order output offsets come from warp ballots.  Rows of at
+// One CTA per row, or a cluster of two that splits the row in halves while
+// two CTAs per row fit in one wave.  Logits become order-preserving 32-bit
+// keys (a larger float gives a larger key; NaN, which only an error row
+// holds, the smallest key).  A histogram of 2,048 linear bins over a sampled
+// range finds the bin of the k-th largest logit (any monotone binning keeps
+// the counts exact); one more pass collects that bin's members into shared
+// memory (usually a handful) and records the positions in higher bins as
+// warp-vote masks.  The collected keys are ranked directly to find the k-th
+// largest key K* and how many keys equal to it are needed (lowest positions
+// first); those taken join the masks, from which the last pass writes the
+// positions in order.  A bin with many members, or a very long row, takes
+// the general path instead: three radix passes (11 + 11 + 10 bits) over the
+// collected keys or the whole row, per-warp counts, and a write that
+// compares every key.  Each warp owns a contiguous segment, its lanes on
+// consecutive float4s, so that shared-memory reads are free of bank
+// conflicts and in-order output offsets come from warp votes.  Rows of at
 // most k valid positions take all of them; the rest of the k outputs is -1
 // (value -inf).
 #include <cooperative_groups.h>
