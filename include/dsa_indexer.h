@@ -38,12 +38,14 @@
  * kscale, when not NULL, is the address of page 0's 64 fp32 scales; page p's
  * are at (char*)kscale + p * page_stride_bytes.  NULL means scale(t) = 1.
  *
- * Common rules for both entry points.
+ * Common rules for the indexer entry points.
  *   Memory.   Every pointer except `stream` is a DEVICE pointer owned by the
- *             caller.  The library allocates nothing, never synchronises and
- *             launches exactly one kernel per call on `stream` (a
- *             cudaStream_t; NULL = legacy default stream).  All calls are
- *             legal inside stream capture.  The kernel is launched with
+ *             caller (the varlen prefill's request offsets are host data).
+ *             The library allocates nothing, never synchronises and
+ *             launches one kernel per call on `stream` (a cudaStream_t;
+ *             NULL = legacy default stream); the top-k calls launch two, the
+ *             varlen prefill one per request.  All calls are legal inside
+ *             stream capture.  Every kernel is launched with
  *             programmatic dependent launch allowed: its set-up may overlap
  *             the tail of the previous kernel in the stream, but it reads no
  *             argument array before that kernel has completed.
@@ -188,8 +190,10 @@ int dsa_indexer_logits_prefill_varlen(const void* q, const float* w, const void*
  * B * W * 64 entries (16-byte aligned) that receives the logits of the valid
  * positions only (no -inf fill, so the output bytes of a long table are not
  * written); the caller owns it.  Two kernel launches on `stream`: the
- * decode kernel, then the selection (one CTA per request, a three-pass
- * radix select).  Other arguments, checks and data errors as for
+ * decode kernel, then the selection (a cluster of two CTAs per request
+ * while 2 * B CTAs fit in one wave of one CTA per SM, else one CTA per
+ * request: a histogram pass, the k-th value's bin collected and ranked, an
+ * in-order write).  Other arguments, checks and data errors as for
  * dsa_indexer_logits_decode; an over-long row selects nothing (all -1) and
  * reports DSA_ERR_BAD_SEQLEN.
  */
