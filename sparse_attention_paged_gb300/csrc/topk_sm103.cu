@@ -59,7 +59,7 @@ struct TopkParams {
   float* vals;           // nullable, same layout
   long long out_stride;
   int* status;
-  int cache_floats;      // rows up to this length are kept in shared memory
+  int cache_floats;      // a CTA's part of a row up to this length is kept in shared memory
 };
 
 __device__ __forceinline__ uint32_t order_key(float v) {
@@ -147,9 +147,9 @@ __device__ __forceinline__ int warp_sum(int v) {
   return v;
 }
 
-// kCl CTAs per row (1, or a cluster of 2 that splits the row in halves and
-// exchanges its range, histogram, collected keys and counts through
-// distributed shared memory).
+// kCl CTAs per row (1, or a cluster of 2 that splits the row in halves:
+// each reads the other's histogram and receives its collected keys and
+// counts through distributed shared memory).
 template <int kCl>
 __global__ void __launch_bounds__(kTkThreads)
     topk_kernel(const TopkParams p) {
@@ -350,9 +350,8 @@ __global__ void __launch_bounds__(kTkThreads)
   // The usual case ("fast": at most kRankMax members and a segment of at
   // most kMaskSteps steps) ranks the collected keys directly and records
   // the positions taken as warp-vote masks, one word per (warp, step,
-  // element of the float4), in the histogram's place (free once bin lb is
-  // known): positions in bins above lb while the row is collected, then the
-  // collected ones that make the cut.
+  // element of the float4): positions in bins above lb while the row is
+  // collected, then the collected ones that make the cut.
   const bool collect = pop <= kCand;
   const int S = (seg4 + 31) >> 5;            // steps of 32 float4s in a warp's segment
   const bool fast = pop <= kRankMax && S <= kMaskSteps;
