@@ -100,3 +100,36 @@ def test_repeated_calls_take_no_device_memory():
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free0
     assert int(dw.status.item()) == 0
+
+
+@pytest.mark.gpu
+def test_static_call_captured_after_its_first_call():
+    """The first call on a device (made above, outside capture) sets the
+    array up; later calls may be captured and replayed with new lengths."""
+    import torch
+    import sparse_attention_paged_gb300 as lib
+    from tests.parity import DeviceWorkload
+    W, k = 50, 128
+    w0 = wl.decode_with_lengths("na3", [2000, 3200, 5, 900], W, seed=23)
+    w1 = wl.decode_with_lengths("na4", [3199, 64, 1700, 129], W, seed=24)
+    dw = DeviceWorkload(w0)
+    idx = torch.empty((w0.R, k), dtype=torch.int32, device="cuda")
+    val = torch.empty((w0.R, k), dtype=torch.float32, device="cuda")
+    args = lambda: (dw.q, dw.wt, dw.kcache, dw.kscale_ptr, w0.page_stride, w0.num_pages,
+                    w0.kv_dtype, dw.bt, w0.bt_stride, dw.seqlens, w0.R, 64, 128, 64, W, k, idx,
+                    val, k, dw.status)
+    assert lib.dsa_indexer_topk_decode_static(*args()) == 0
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        lib.dsa_indexer_topk_decode_static(*args())
+    for w in (w0, w1):
+        src = DeviceWorkload(w)
+        for name in ("q", "wt", "kcache", "bt", "seqlens"):
+            getattr(dw, name).copy_(getattr(src, name))
+        g.replay()
+        torch.cuda.synchronize()
+        got = (idx.cpu().numpy().copy(), val.cpu().numpy().copy())
+        _, ((i0, v0), _) = _run_both(w, k)
+        assert np.array_equal(got[0], i0)
+        assert np.array_equal(got[1].view(np.uint32), v0.view(np.uint32))
