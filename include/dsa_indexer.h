@@ -177,7 +177,6 @@ int dsa_indexer_logits_prefill_varlen(const void* q, const float* w, const void*
                                       float* out, long long out_stride, int* dev_status,
                                       void* stream);
 
-/* A static, human-readable name for a status code. */
 /*
  * Decode with top-k selection: for every request b, the k_top positions
  * t < seqlens[b] with the largest logits (the positions sparse attention
@@ -206,16 +205,23 @@ int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
                             void* stream);
 
 /*
- * dsa_indexer_topk_decode without a caller workspace: the logits go to a
- * fixed device array of the library (24 Mi floats, 96 MiB, held by the
- * process once this entry point is first used).  Nothing is allocated by
- * the call.  B * W * 64 must not exceed 24 Mi (DSA_ERR_UNSUPPORTED
- * otherwise, checked before any device work).  The array is shared: calls
- * on one device must not overlap (use one stream, or order the streams);
- * the first call on a device looks up the array's address (which may load
- * its module), so make one call before capturing one in a CUDA graph.  The
- * pages have no counterpart: this is a convenience of the library.  Other
- * arguments and results as for dsa_indexer_topk_decode.
+ * dsa_indexer_topk_decode without a caller workspace, for callers that
+ * cannot allocate device memory for it (an allocator that is not theirs to
+ * call, a memory pool fixed at start-up, code running inside another
+ * library's allocation-free hot path).  The logits go to a fixed device
+ * array of the library (24 Mi floats, 96 MiB per device); the call itself
+ * allocates nothing.  With lazy module loading (the CUDA default) the array
+ * is reserved on a device when this entry point is first used there; under
+ * CUDA_MODULE_LOADING=EAGER every process that loads the library reserves
+ * it on every device it creates a context on, whether or not it calls this.
+ * B * W * 64 must not exceed 24 Mi (DSA_ERR_UNSUPPORTED otherwise, checked
+ * before any device work).  The array is shared: calls on one device must
+ * not overlap (use one stream, or order the streams), or they race.  The
+ * first call with B > 0 on a device looks up the array's address (which may
+ * load its module), so make one such call before capturing one in a CUDA
+ * graph.  The pages have no counterpart: this is a convenience of the
+ * library.  Every other argument is checked, and every result written, as
+ * by dsa_indexer_topk_decode.
  */
 int dsa_indexer_topk_decode_static(const void* q, const float* w, const void* kcache,
                                    const void* kscale, long long page_stride_bytes,
@@ -251,6 +257,7 @@ int dsa_kcache_store(const void* k, const int* slot_mapping, int n, void* kcache
                      long long page_stride_bytes, int num_pages, int kv_dtype,
                      int D, int page_size, int* dev_status, void* stream);
 
+/* A static, human-readable name for a status code. */
 const char* dsa_status_string(int status);
 
 /* DSA_INDEXER_ABI_VERSION of the loaded library. */

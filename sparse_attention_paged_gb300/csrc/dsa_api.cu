@@ -194,16 +194,18 @@ int dsa_indexer_topk_decode_static(const void* q, const float* w, const void* kc
                                    int page_size, int W, int k_top, int* topk_idx,
                                    float* topk_val, long long topk_stride, int* dev_status,
                                    void* stream) {
-  // size first: an oversized call is refused before any device work
-  if (B < 0 || W < 1) return DSA_ERR_INVALID_ARG;
-  if ((long long)B * W * dsa::kPage > dsa::static_scratch_floats()) return DSA_ERR_UNSUPPORTED;
-  if (B == 0) return DSA_OK;
+  // size first: an oversized call is refused before any device work; every
+  // other argument is checked by the workspace entry point, as for a call
+  // with a caller workspace (B = 0 passes no workspace and launches nothing)
+  if (B > 0 && W > 0 && (long long)B * W * dsa::kPage > dsa::static_scratch_floats())
+    return DSA_ERR_UNSUPPORTED;
   float* ws = nullptr;
-  if (dsa::static_scratch(&ws) != cudaSuccess) return DSA_ERR_CUDA;
+  if (B > 0 && W > 0 && dsa::static_scratch(&ws) != cudaSuccess) return DSA_ERR_CUDA;
   return dsa_indexer_topk_decode(q, w, kcache, kscale, page_stride_bytes, num_pages, kv_dtype,
                                  block_table, bt_stride, seqlens, B, H, D, page_size, W, k_top,
                                  topk_idx, topk_val, topk_stride, ws,
-                                 dsa::static_scratch_floats(), dev_status, stream);
+                                 ws != nullptr ? dsa::static_scratch_floats() : 0, dev_status,
+                                 stream);
 }
 
 int dsa_kcache_store(const void* k, const int* slot_mapping, int n, void* kcache,

@@ -152,6 +152,28 @@ def _rows(g: torch.Generator, R: int) -> tuple[np.ndarray, np.ndarray]:
     return q, w
 
 
+def wide_range_queries(R: int, seed: int, outlier_d: int | None = None) -> np.ndarray:
+    """bf16 query bits [R, H, D] whose heads span a wide dynamic range:
+    every head has a magnitude m = 2^U{-3..3} and one outlier element of
+    magnitude 256 * m with a random sign (at a random index, or at
+    `outlier_d` in every head); the other elements are sign * m * 2^U[-6, 0],
+    so they reach down to 2^-14 of the head's largest, one in eight of them
+    exactly zero; every 16th head is all zero."""
+    g = _gen(seed)
+    mag = 2.0 ** torch.randint(-3, 4, (R, H, 1), generator=g).double()
+    sign = torch.sign(torch.randn(R, H, D, generator=g, dtype=torch.float64))
+    x = sign * mag * 2.0 ** (-6.0 * torch.rand(R, H, D, generator=g, dtype=torch.float64))
+    x[torch.rand(R, H, D, generator=g) < 0.125] = 0.0
+    if outlier_d is None:
+        idx = torch.randint(0, D, (R, H, 1), generator=g)
+    else:
+        idx = torch.full((R, H, 1), int(outlier_d), dtype=torch.int64)
+    osign = torch.sign(torch.randn(R, H, 1, generator=g, dtype=torch.float64))
+    x.scatter_(2, idx, osign * mag * 256.0)
+    x[:, ::16, :] = 0.0
+    return _bf16_bits(x.float())
+
+
 def _used_pages(bt: np.ndarray, seqlens: np.ndarray, bt_stride: int) -> np.ndarray:
     used = []
     for r in range(len(seqlens)):
@@ -443,6 +465,8 @@ def cfg7() -> Workload:
 NAMED = {
     "1": lambda: [cfg1()],
     "2": lambda: [cfg2a(), cfg2b()],
+    "2a": lambda: [cfg2a()],
+    "2b": lambda: [cfg2b()],
     "3": lambda: [cfg3(4097)],
     "3ref": lambda: [cfg3(512)],
     "3short": lambda: [cfg3_short(4097)],

@@ -31,3 +31,51 @@ def test_call_objects(name):
         if w.kind != "store":
             assert c.host_table().shape[1] == w.W
         assert c.nbytes() > 0
+
+
+def test_sweep_covers_every_configuration():
+    """The per-configuration records name every configuration of the five
+    (both calls of config 2, config 3 at both widths, the short lengths
+    capped and uncapped)."""
+    assert set(bench.SWEEP) <= set(wl.NAMED)
+    assert {"1", "2a", "2b", "3", "3ref", "3short", "3short_capped", "4", "5"} == set(bench.SWEEP)
+    for name in bench.SWEEP:
+        assert len(wl.NAMED[name]()) == 1
+
+
+def test_rotating_copies_exceed_twice_the_l2():
+    for name in ("1", "2b", "3", "4"):
+        works = wl.NAMED[name]()
+        n = bench.n_copies_for(works)
+        assert n * sum(w.algorithmic_bytes() for w in works) > 2 * bench.L2_BYTES
+
+
+def test_stacked_copies_are_independent_views():
+    torch = pytest.importorskip("torch")
+    w = wl.cfg2b()
+    copies = bench.make_copies([w], torch.device("cpu"), 3)
+    ptrs = set()
+    for cs in copies:
+        c = cs[0]
+        assert c.q.shape == (w.R, 64, 128) and c.out.shape == (w.R, w.W * 64)
+        assert bool((c.seqlens.numpy() == w.seqlens).all())
+        assert bytes(c.kcache.numpy()) == bytes(w.kcache)
+        for t in (c.q, c.wt, c.kcache, c.bt, c.seqlens, c.out, c.status):
+            assert t.data_ptr() % 16 == 0
+            ptrs.add(t.data_ptr())
+        assert c.kscale == c.kcache.data_ptr() + w.kscale_offset
+    assert len(ptrs) == 3 * 7
+
+
+def test_roofline_record_bounds():
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1700.0}
+    w4 = wl.cfg4()
+    us = w4.algorithmic_bytes() / 6000e9 * 1e6 * 2          # half the HBM peak
+    r = bench.roofline_record(w4, us, peaks)
+    assert r["bound"] == "hbm" and abs(r["frac"] - 0.5) < 1e-9
+    assert abs(r["t_roof_us"] - us / 2) < 1e-6
+    w5 = wl.cfg5()
+    us = w5.flops() / 2000e12 * 1e6 / 0.75
+    r = bench.roofline_record(w5, us, peaks)
+    assert r["bound"] == "tensor" and abs(r["frac"] - 0.75) < 1e-9
+    assert abs(r["frac_sustained"] - 0.75 * 2000 / 1700) < 1e-9

@@ -201,17 +201,47 @@ def _sampled(w, rows):
     return compare(o[rows], ref)
 
 
-def test_config4_bf16_full_size_sampled_rows():
-    w = wl.cfg4()
-    L = w.seqlens
-    rows = sorted(set([int(np.argmin(L)), int(np.argmax(L)), 0, 1, 31, 63]))
-    _sampled(w, rows)
+def test_config4_bf16_full_size_all_rows():
+    """All 64 requests of the bf16 decode configuration, every position."""
+    stats = _check_full(wl.cfg4())
+    assert stats["rel"] < 1e-3
+
+
+def config5_rows(n_sms: int) -> list[int]:
+    """Rows of the full-size prefill to compare value by value: the first
+    and the last query of every 16th query tile, and of the query tiles
+    where each persistent CTA's slice of the (query tile, position tile)
+    item list starts and ends (the kernel splits the list evenly over one
+    CTA per SM, so these rows sit at every CTA's boundaries)."""
+    w = wl.cfg5()
+    T = w.W * w.P
+    L = np.where(w.seqlens > T, 0, np.clip(w.seqlens, 0, T)).astype(np.int64)
+    n_qt = (w.R + 3) // 4
+    lmax = np.array([L[4 * j: 4 * j + 4].max() for j in range(n_qt)])
+    tiles = (lmax + 127) // 128
+    cum = np.concatenate([[0], np.cumsum(tiles)])
+    total = int(cum[-1])
+    rows = set()
+    for j in range(0, n_qt, 16):
+        rows.update((4 * j, min(4 * j + 3, w.R - 1)))
+    for k in range(n_sms):
+        a = k * total // n_sms
+        b = (k + 1) * total // n_sms - 1
+        if b < a:
+            continue
+        for item in (a, b):
+            j = int(np.searchsorted(cum, item, side="right") - 1)
+            rows.update((4 * j, min(4 * j + 3, w.R - 1)))
+    rows.update((0, w.R - 1))
+    return sorted(rows)
 
 
 def test_config5_prefill_full_size_sampled_rows():
-    w = wl.cfg5()
-    rows = [0, 1, 2, 3, 127, 128, 1000, 2047, 2048, 3001, 4094, 4095]
-    _sampled(w, rows)
+    import torch
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = config5_rows(n_sms)
+    assert len(rows) >= 256
+    _sampled(wl.cfg5(), rows)
 
 
 @pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_E4M3])
@@ -344,3 +374,46 @@ def test_many_rows_long_table_natural_order():
     g = np.random.default_rng(13)
     lengths = g.integers(0, 65 * 64 + 1, 400)
     _check_full(wl.decode_with_lengths("many", lengths, 65, seed=13))
+
+
+# --- queries with a wide dynamic range per head: the fp8 path represents the
+# bf16 query as two e4m3 terms under a per-head power-of-two scale; elements
+# far below their head's largest are where that representation is least
+# exact ----------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_decode_fp8_wide_range_queries(seed):
+    for w in (wl.decode_uniform(f"wr{seed}", 16, 32, 2048, 512, seed=40 + seed),
+              wl.decode_with_lengths(f"wrl{seed}", [0, 1, 64, 65, 3000, 90 * 64],
+                                     90, seed=42 + seed)):
+        w.q_bits = wl.wide_range_queries(w.R, seed=50 + seed)
+        stats = _check_full(w)
+        assert stats["rel"] < 1e-3
+
+
+def test_prefill_fp8_wide_range_queries():
+    w = wl.prefill_causal("pf_wr", 130, 10, 10 * 64 - 140, seed=43, kv_dtype=wl.KV_E4M3)
+    w.q_bits = wl.wide_range_queries(w.R, seed=52)
+    _check_full(w)
+
+
+def test_prefill_and_decode_bf16_wide_range_queries():
+    for w in (wl.prefill_causal("pf_wr_bf", 70, 9, 9 * 64 - 75, seed=44),
+              wl.decode_uniform("wr_bf", 8, 12, 12 * 64, 200, seed=45, kv_dtype=wl.KV_BF16)):
+        w.q_bits = wl.wide_range_queries(w.R, seed=53)
+        _check_full(w)
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_E4M3])
+@pytest.mark.parametrize("exp", [-40, 30])
+def test_prefill_tiny_and_large_dots(kv, exp):
+    """Queries scaled by 2^-40 (per-head dots near 2^-37) and by 2^30 (dots
+    near 2^33): half of the heads take their ReLU as a saturating multiply
+    by 2^-64, whose products must stay normal floats at the small end and
+    below 1 at the large end."""
+    import torch
+    w = wl.prefill_causal(f"pf_sc{exp}", 40, 6, 6 * 64 - 50, seed=46, kv_dtype=kv)
+    q = torch.from_numpy(w.q_bits.view(np.int16)).view(torch.bfloat16).float() * (2.0 ** exp)
+    w.q_bits = q.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    stats = _check_full(w)
+    assert stats["max_ref"] > 0

@@ -1,10 +1,15 @@
-"""The top-k entry point that allocates nothing (its logits go to a fixed
-device array of the library).  Collected last: its first GPU call loads the
-array's module and reserves the array for the rest of the process.
+"""The top-k entry point that allocates nothing, for callers that cannot
+allocate device memory for a workspace (its logits go to a fixed device
+array of the library).  The file name sorts last, so that a run stopping at
+its first failure has run every other test first; the tests themselves do
+not depend on their order (free memory is read after the call that sets the
+array up).
 
-Host part: the entry point is exported and refuses an oversized call before
-any device work.  GPU part: results bit-identical to the workspace entry
-point, and no device memory taken by repeated calls."""
+Host part: the entry point is exported, refuses an oversized call before any
+device work and validates every other argument as the workspace entry point
+does.  GPU part: on two calls in a row, results bit-identical to the
+workspace entry point's and a valid top-k against the oracle's logits; no
+device memory taken by repeated calls; capture after the first call."""
 import os
 import shutil
 
@@ -46,6 +51,12 @@ def test_oversized_call_is_refused_before_device_work():
     assert _call(lib, B=64, W=6145, bt_stride=6145) == 2
     assert _call(lib, B=0) == 0
     assert _call(lib, B=-1) == 1
+    # with no rows nothing is launched, but the other arguments are still
+    # checked as the workspace entry point checks them
+    assert _call(lib, B=0, H=32) == 2
+    assert _call(lib, B=0, kv_dtype=5) == 1
+    assert _call(lib, B=0, k_top=0) == 1
+    assert _call(lib, B=0, W=0) == 1
 
 
 def _run_both(w, k):
@@ -73,11 +84,17 @@ def _run_both(w, k):
 
 @pytest.mark.gpu
 def test_static_matches_the_workspace_call():
+    from tests.test_gpu_topk import _check
     for w, k in [(wl.decode_with_lengths("na", [0, 5, 700, 2000], 40, seed=21), 64),
                  (wl.cfg3(4097), 2048)]:
         _, ((i0, v0), (i1, v1)) = _run_both(w, k)
         assert np.array_equal(i0, i1)
         assert np.array_equal(v0.view(np.uint32), v1.view(np.uint32))
+        # the static call's own result is a valid top-k of the oracle's logits
+        L = w.seqlens
+        rows = (list(range(w.R)) if w.R <= 8 else
+                sorted({int(np.argmin(L)), int(np.argmax(L)), 0, w.R - 1}))
+        _check(w, k, i1, v1, rows)
 
 
 @pytest.mark.gpu
