@@ -55,6 +55,7 @@ WORKLOAD_DESC = {
     "3short": "decode fp8 B=64 W=4097 L log-uniform 512..2048",
     "3short_capped": "decode fp8 B=64 W=32 L log-uniform 512..2048",
     "4": "decode bf16 B=64 W=2048 L log-uniform 4096..131072",
+    "4s": "decode bf16 B=64 W=512 L log-uniform 1024..32768 (config 4's kernel, profile-sized)",
     "5": "prefill bf16 n_q=4096 W=352 causal limit 18432+i",
     "6": "prefill bf16, 4 requests (query tokens, context) = (256, 6144), (512, 12288), "
          "(128, 3072), (1024, 20480), per-query table rows",
@@ -63,11 +64,13 @@ WORKLOAD_DESC = {
     "7": "prefill fp8 n_q=1024 W=128 causal limit 7168+i",
     "8": "key-cache store: 65536 bf16 key rows into e4m3 pages (+ scales), random slots of 2048 pages",
     "9": "decode fp8 B=64 W=4097 L log-uniform 512..32768, top-2048 positions per request",
+    "9k256": "decode fp8 B=64 W=4097 L log-uniform 512..32768, top-256 positions per request",
+    "9k512": "decode fp8 B=64 W=4097 L log-uniform 512..32768, top-512 positions per request",
 }
 # default (steps, warmup): a timed region of roughly one second per GPU
 DEFAULT_STEPS = {"1": 100000, "2": 100000, "2a": 100000, "2b": 100000, "3": 20000, "3ref": 20000, "3short": 40000,
-                 "3short_capped": 100000, "4": 10000, "5": 1000, "6": 2000, "6v": 2000, "7": 5000,
-                 "8": 10000, "9": 20000}
+                 "3short_capped": 100000, "4": 10000, "4s": 40000, "5": 1000, "6": 2000, "6v": 2000, "7": 5000,
+                 "8": 10000, "9": 20000, "9k256": 20000, "9k512": 20000}
 METRIC = "indexer key-positions scored/s & achieved HBM GB/s (frac of roofline), 1 GB300"
 
 

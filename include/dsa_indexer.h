@@ -177,6 +177,13 @@ int dsa_indexer_logits_prefill_varlen(const void* q, const float* w, const void*
                                       float* out, long long out_stride, int* dev_status,
                                       void* stream);
 
+/* How the top-k decode computes its selection (dsa_indexer_topk_decode_form). */
+typedef enum {
+  DSA_TOPK_AUTO = 0,      /* the fused form where it applies, else two passes */
+  DSA_TOPK_TWO_PASS = 1,  /* the logits into the workspace, then a selection kernel */
+  DSA_TOPK_FUSED = 2      /* selection in the decode epilogue, then a merge kernel */
+} dsa_topk_form_t;
+
 /*
  * Decode with top-k selection: for every request b, the k_top positions
  * t < seqlens[b] with the largest logits (the positions sparse attention
@@ -186,15 +193,27 @@ int dsa_indexer_logits_prefill_varlen(const void* q, const float* w, const void*
  * them and pads with -1.  topk_val (nullable): their logits, same layout,
  * -inf for the padding.  Equal logits at the k-th place are taken in
  * position order.  workspace: device fp32 buffer of at least
- * B * W * 64 entries (16-byte aligned) that receives the logits of the valid
- * positions only (no -inf fill, so the output bytes of a long table are not
- * written); the caller owns it.  Two kernel launches on `stream`: the
- * decode kernel, then the selection (a cluster of two CTAs per request
- * while 2 * B CTAs fit in one wave of one CTA per SM, else one CTA per
- * request: a histogram pass, the k-th value's bin collected and ranked, an
- * in-order write).  Other arguments, checks and data errors as for
- * dsa_indexer_logits_decode; an over-long row selects nothing (all -1) and
- * reports DSA_ERR_BAD_SEQLEN.
+ * B * W * 64 entries (16-byte aligned), owned by the caller; no -inf fill
+ * is written anywhere.  Two kernel launches on `stream`, in one of two
+ * forms (the fused one where it applies):
+ *   two passes: the decode kernel writes the logits of the valid positions
+ *     into the workspace, then the selection kernel (a cluster of two CTAs
+ *     per request while 2 * B CTAs fit in one wave of one CTA per SM, else
+ *     one CTA per request: a histogram pass, the k-th value's bin collected
+ *     and ranked, an in-order write) reads them;
+ *   fused: the decode kernel keeps the logits in shared memory, chunk by
+ *     chunk of up to 32 pages of a row, and writes each chunk's best
+ *     min(k_top, n) positions with their logits to the workspace; a merge
+ *     kernel then selects each request's best among them.  No logit of the
+ *     call is written to global memory.  It applies when k_top <= 1024, the
+ *     decode takes its balanced form (W > 64 and B <= 384) and the
+ *     workspace holds 4 * ceil((B + 1) / 4) + (C + B + ceil(B * W / 32)) *
+ *     (4 + 2 * k_top) floats, C being the decode's persistent CTAs (two per
+ *     SM).
+ * Both forms take the same positions and return the same logits, bit for
+ * bit: the logits come from the same arithmetic and the order is total.
+ * Other arguments, checks and data errors as for dsa_indexer_logits_decode;
+ * an over-long row selects nothing (all -1) and reports DSA_ERR_BAD_SEQLEN.
  */
 int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
                             const void* kscale, long long page_stride_bytes, int num_pages,
@@ -203,6 +222,21 @@ int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
                             int k_top, int* topk_idx, float* topk_val, long long topk_stride,
                             float* workspace, long long workspace_floats, int* dev_status,
                             void* stream);
+
+/*
+ * dsa_indexer_topk_decode with the form chosen by the caller (a
+ * dsa_topk_form_t; DSA_ERR_INVALID_ARG for another value).  DSA_TOPK_FUSED
+ * where the fused form does not apply returns DSA_ERR_UNSUPPORTED before
+ * any launch.  The top-k is the logits' consumer: "The Dispatch Decision
+ * ...", section "The Problem That Led Here".
+ */
+int dsa_indexer_topk_decode_form(const void* q, const float* w, const void* kcache,
+                                 const void* kscale, long long page_stride_bytes, int num_pages,
+                                 int kv_dtype, const int* block_table, long long bt_stride,
+                                 const int* seqlens, int B, int H, int D, int page_size, int W,
+                                 int k_top, int* topk_idx, float* topk_val, long long topk_stride,
+                                 float* workspace, long long workspace_floats, int* dev_status,
+                                 int form, void* stream);
 
 /*
  * dsa_indexer_topk_decode without a caller workspace, for callers that

@@ -116,6 +116,23 @@ def dsa_indexer_topk_decode(q, w, kcache, kscale, page_stride_bytes, num_pages, 
         _p(workspace), int(workspace_floats), _p(dev_status), _stream(stream)))
 
 
+TOPK_AUTO = 0
+TOPK_TWO_PASS = 1
+TOPK_FUSED = 2
+
+
+def dsa_indexer_topk_decode_form(q, w, kcache, kscale, page_stride_bytes, num_pages, kv_dtype,
+                                 block_table, bt_stride, seqlens, B, H, D, page_size, W, k_top,
+                                 topk_idx, topk_val, topk_stride, workspace, workspace_floats,
+                                 dev_status=None, form=TOPK_AUTO, stream=None) -> int:
+    """C ``dsa_indexer_topk_decode_form``; returns its status code."""
+    return int(_native.load().dsa_indexer_topk_decode_form(
+        _p(q), _p(w), _p(kcache), _p(kscale), int(page_stride_bytes), int(num_pages),
+        int(kv_dtype), _p(block_table), int(bt_stride), _p(seqlens), int(B), int(H), int(D),
+        int(page_size), int(W), int(k_top), _p(topk_idx), _p(topk_val), int(topk_stride),
+        _p(workspace), int(workspace_floats), _p(dev_status), int(form), _stream(stream)))
+
+
 def dsa_indexer_topk_decode_static(q, w, kcache, kscale, page_stride_bytes, num_pages,
                                    kv_dtype, block_table, bt_stride, seqlens, B, H, D,
                                    page_size, W, k_top, topk_idx, topk_val, topk_stride,

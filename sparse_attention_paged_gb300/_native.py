@@ -27,6 +27,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
 # Every symbol include/dsa_indexer.h declares.
 EXPORTS = ("dsa_indexer_logits_decode", "dsa_indexer_logits_prefill",
            "dsa_indexer_logits_prefill_varlen", "dsa_indexer_topk_decode",
+           "dsa_indexer_topk_decode_form",
            "dsa_indexer_topk_decode_static", "dsa_kcache_store",
            "dsa_status_string", "dsa_indexer_abi_version")
 
@@ -103,6 +104,10 @@ def load() -> ctypes.CDLL:
         lib.dsa_indexer_topk_decode.restype = ci
         lib.dsa_indexer_topk_decode.argtypes = [vp, vp, vp, vp, ll, ci, ci, vp, ll, vp, ci, ci,
                                                 ci, ci, ci, ci, vp, vp, ll, vp, ll, vp, vp]
+        lib.dsa_indexer_topk_decode_form.restype = ci
+        lib.dsa_indexer_topk_decode_form.argtypes = [vp, vp, vp, vp, ll, ci, ci, vp, ll, vp, ci,
+                                                     ci, ci, ci, ci, ci, vp, vp, ll, vp, ll, vp,
+                                                     ci, vp]
         lib.dsa_indexer_logits_prefill_varlen.restype = ci
         lib.dsa_indexer_logits_prefill_varlen.argtypes = [vp, vp, vp, vp, ll, ci, ci, vp, ll, vp,
                                                           ci, vp, ci, ci, ci, ci, vp, ll, vp, vp]

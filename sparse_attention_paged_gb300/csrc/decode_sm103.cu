@@ -48,6 +48,7 @@
 #include "dsa_common.cuh"
 #include "sm100_ptx.cuh"
 #include "tensor_maps.cuh"
+#include "topk_slots.cuh"
 
 namespace dsa {
 
@@ -111,10 +112,25 @@ constexpr int kCtrlPv = kCtrlLens + 4 * kMaxRowsBalanced;
 constexpr int kCtrlPf = kCtrlPv + 4 * (kMaxRowsBalanced + 1);
 constexpr int kCtrlBytes = kCtrlPf + 4 * (kMaxRowsBalanced + 1);
 
+// The auxiliary region: with the fill, blocks of -inf and of NaN (the
+// sources of the bulk copies that write it); with the fused top-k, a chunk's
+// logits, a 256-bin histogram and scan scratch.
+constexpr int kFillBlock = 4096;
+constexpr int kNanBlock = 1024;
+// The fill's bulk copies go out in step with the page loads (a share after
+// each tile from the S-th on) rather than all at once, so that DRAM serves a
+// steady mix of reads and writes and no load waits behind the whole fill.
+constexpr bool kFillPaced = true;
+constexpr int kSelHist = kSelChunk * 4;            // byte offsets in the region
+constexpr int kSelScratch = kSelHist + 256 * 4;
+constexpr int kSelBytes = kSelScratch + 64;
+constexpr int kAuxBytes = kSelBytes > kFillBlock + kNanBlock ? kSelBytes : kFillBlock + kNanBlock;
+
 template <int KV>
 constexpr int dec_smem_bytes() {
   using C = DecCfg<KV>;
-  return 1024 /* alignment slack */ + 2 * C::kQBytes + C::kStages * C::kTileBytes + kCtrlBytes;
+  return 1024 /* alignment slack */ + 2 * C::kQBytes + C::kStages * C::kTileBytes + kAuxBytes +
+         kCtrlBytes;
 }
 
 __device__ __forceinline__ float nanf_() { return __int_as_float(0x7fc00000); }
@@ -227,6 +243,108 @@ struct Tiles {
   }
 };
 
+// Barrier of the four epilogue warps.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Exclusive prefix sum over the 128 epilogue threads (four warps); `scr`
+// holds 4 ints.  Returns this thread's prefix; *total gets the sum.
+__device__ __forceinline__ int epi_scan(int v, int* scr, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scr[w] = x;
+  epi_sync();
+  int base = 0, sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = scr[j];
+    if (j < w) base += c;
+    sum += c;
+  }
+  epi_sync();                                 // scr may be reused at once
+  *total = sum;
+  return base + x - v;
+}
+
+// A complete chunk of the fused top-k: its n logits are buf[0, n) (position
+// p0 + i at i).  Writes its best min(k, n) -- largest logit first, lower
+// position first among equal logits -- into `slot` in position order, with
+// the count.  The k-th best key is found by radix selection, 8 bits a pass
+// over a 256-bin histogram.  Called by the 128 epilogue threads together.
+__device__ void select_chunk(const float* buf, int n, int p0, int k, float* slot, int* hist,
+                             int* scr) {
+  const int tid = threadIdx.x;
+  float* vals = slot + kSlotHead;
+  int* poss = reinterpret_cast<int*>(slot + kSlotHead + k);
+  if (n <= k) {
+    for (int i = tid; i < n; i += 128) {
+      vals[i] = buf[i];
+      poss[i] = p0 + i;
+    }
+    if (tid == 0) *reinterpret_cast<int*>(slot) = n;
+    return;
+  }
+  uint32_t prefix = 0, mask = 0;
+  int need = k;                               // still to take among keys matching prefix
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    hist[tid] = 0;
+    hist[tid + 128] = 0;
+    epi_sync();
+    for (int i = tid; i < n; i += 128) {
+      const uint32_t key = sel_key(buf[i]);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+    }
+    epi_sync();
+    const int d1 = 255 - 2 * tid, d0 = d1 - 1;   // this thread's digits, high first
+    const int h1 = hist[d1], h0 = hist[d0];
+    int tot;
+    const int before = epi_scan(h1 + h0, scr, &tot);   // keys in higher digits
+    if (before < need && before + h1 >= need) {
+      scr[4] = d1;
+      scr[5] = before;
+    } else if (before + h1 < need && before + h1 + h0 >= need) {
+      scr[4] = d0;
+      scr[5] = before + h1;
+    }
+    epi_sync();
+    const uint32_t digit = (uint32_t)scr[4];
+    need -= scr[5];
+    prefix |= digit << shift;
+    mask |= 0xFFu << shift;
+    epi_sync();                               // hist and scr[4..5] are reused
+  }
+  // prefix is the k-th best key; `need` keys equal to it are taken, the
+  // lowest positions first.  Thread t writes [16t, 16t + 16) in order.
+  const int i0 = 16 * tid, i1 = min(i0 + 16, n);
+  int gt = 0, eq = 0;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = sel_key(buf[i]);
+    gt += key > prefix;
+    eq += key == prefix;
+  }
+  int tot;
+  const int eq_before = epi_scan(eq, scr, &tot);
+  const int eq_take = min(max(need - eq_before, 0), eq);
+  int o = epi_scan(gt + eq_take, scr, &tot);
+  int e = eq_before;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = sel_key(buf[i]);
+    bool take = key > prefix;
+    if (key == prefix) take = e++ < need;
+    if (take) {
+      vals[o] = buf[i];
+      poss[o] = p0 + i;
+      ++o;
+    }
+  }
+  if (tid == 0) *reinterpret_cast<int*>(slot) = k;
+}
+
 }  // namespace
 
 template <int KV>
@@ -240,7 +358,10 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
                                              ~uintptr_t(1023));
   uint8_t* sQ = smem;                          // 2 x B operand (row segments alternate)
   uint8_t* sA = smem + 2 * C::kQBytes;         // A stages
-  uint8_t* ctrl = sA + S * C::kTileBytes;
+  uint8_t* sAux = sA + S * C::kTileBytes;    // [kAuxBytes]
+  uint8_t* sInf = sAux;                       // fill: [kFillBlock] -inf
+  uint8_t* sNan = sAux + kFillBlock;          // fill: [kNanBlock] NaN
+  uint8_t* ctrl = sAux + kAuxBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;                 // [2] accumulator ready
@@ -279,32 +400,131 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   griddep_wait();
   griddep_launch_dependents();
 
+  // fp8 query split, done by warps 0-3 (warp w owns heads 16w..16w+15, lane
+  // l owns d = 4l..4l+3): q_load fetches row r's query and head weights,
+  // q_convert writes q * 2^e_h = hi + lo into query buffer sb as two e4m3
+  // terms (K-major, 128-byte swizzle) and the weights w_h * 2^-e_h
+  auto q_load = [&](int r, uint2 (&raw)[16], float& wv) {
+    const uint16_t* qrow = p.q + (long long)r * kHeads * kDim;
+#pragma unroll
+    for (int hh = 0; hh < 16; ++hh)
+      raw[hh] = __ldg(reinterpret_cast<const uint2*>(qrow + (warp * 16 + hh) * kDim) + lane);
+    wv = lane < 16 ? __ldg(p.w + (long long)r * kHeads + warp * 16 + lane) : 0.f;
+  };
+  auto q_convert = [&](const uint2 (&raw)[16], float wv, int sb) {
+    float* ws = w_s + sb * kHeads;
+    uint8_t* qb = sQ + sb * C::kQBytes;
+#pragma unroll
+    for (int hh = 0; hh < 16; ++hh) {
+      const int h = warp * 16 + hh;
+      float x[4] = {bf16f(raw[hh].x & 0xffffu), bf16f(raw[hh].x >> 16),
+                    bf16f(raw[hh].y & 0xffffu), bf16f(raw[hh].y >> 16)};
+      float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+      m = warp_max(m);
+      int e = 0;
+      if (m > 0.f) {
+        const int E = ((__float_as_int(m) >> 23) & 0xff) - 127;   // floor(log2 m), m normal
+        e = min(max(7 - E, -126), 126);
+      }
+      const float sc = exp2i(e);
+      uint32_t hi = 0, lo = 0;
+#pragma unroll
+      for (int j = 0; j < 4; j += 2) {
+        const float a0 = x[j] * sc, a1 = x[j + 1] * sc;
+        float h0, h1, l0, l1;
+        const uint32_t hc = to_e4m3x2(a0, a1, h0, h1);
+        const uint32_t lc = to_e4m3x2(a0 - h0, a1 - h1, l0, l1);
+        hi |= hc << (8 * j);
+        lo |= lc << (8 * j);
+      }
+      // row h, bytes [4*lane, 4*lane+4) of 128, 128-byte swizzle
+      const uint32_t off = h * 128 + ((((lane >> 2) ^ (h & 7)) << 4) | ((lane & 3) << 2));
+      *reinterpret_cast<uint32_t*>(qb + off) = hi;
+      *reinterpret_cast<uint32_t*>(qb + 8192 + off) = lo;
+      const float wh = __shfl_sync(0xffffffffu, wv, hh);
+      if (lane == 0) ws[h] = wh * exp2i(-e);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&qbar[sb]);
+  };
+  uint2 q0raw[16];           // fp8: the first segment's query, loaded before the fill
+  float q0w = 0.f;
+
+  // This CTA's share of the fill.  Per-request mode: floats [fill_beg,
+  // fill_end) of row blockIdx.y; balanced mode: fill pages [fill_f0,
+  // fill_f1) of the call (Pf holds the rows' fill-page prefix sums).
+  long long fill_beg = 0, fill_end = 0;
+  bool fill_bad = false;
+  int fill_f0 = 0, fill_f1 = 0;
+  int my_pages = 0;                   // pages this CTA loads (pacing of the fill)
+
+  // Calls f(first float, count, over-long row) for each contiguous piece of
+  // this CTA's share of the fill (each starts 16-byte aligned and counts a
+  // multiple of 4 floats); raises DSA_ERR_BAD_SEQLEN for an over-long row.
+  auto for_each_fill_range = [&](bool report, auto&& f) {
+    if (!balanced) {
+      if (fill_end > fill_beg)
+        f(p.out + (long long)blockIdx.y * p.out_stride + fill_beg, fill_end - fill_beg, fill_bad);
+      return;
+    }
+    const int B = p.rows;
+    if (fill_f0 >= fill_f1) return;
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {      // row holding fill page fill_f0
+      const int mid = (lo + hi + 1) >> 1;
+      if (Pf[mid] <= fill_f0) lo = mid; else hi = mid - 1;
+    }
+    for (int r = lo, fp = fill_f0; fp < fill_f1 && r < B; ++r) {
+      const int nf = Pf[r + 1] - Pf[r];
+      if (nf == 0) continue;
+      const int a = fp - Pf[r];                      // first fill page of row r in range
+      const int e = min(fill_f1 - Pf[r], nf);        // one past the last
+      const bool bad = lens_s[r] > T;
+      const int first_page = p.W - nf;               // = valid pages of row r
+      f(p.out + (long long)r * p.out_stride + (long long)(first_page + a) * kPage,
+        (long long)(e - a) * kPage, bad);
+      if (bad && a == 0 && report) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
+      fp = Pf[r] + e;
+    }
+  };
+
   Tiles tiles;
+  int pre_ph0 = -1, pre_ph1 = -1;     // producer: the first tile's page ids, if loaded early
   if (!balanced) {
     // ---------------------------------------------------------------- per-request
     const int b = blockIdx.y, c = blockIdx.x;
+    if (tid == 128) {
+      // issued before the length arrives, so that the two loads overlap;
+      // used only for pages below the length
+      const int* btrow = p.block_table + (long long)b * p.bt_stride;
+      pre_ph0 = __ldg(btrow + c);
+      if (c + G < p.W) pre_ph1 = __ldg(btrow + c + G);
+    }
     const int L = __ldg(p.seqlens + b);
     const int npv = valid_pages(L, p.W);
     const int n_mine = npv > c ? (npv - 1 - c) / G + 1 : 0;
-    if (tid < 128 || n_mine == 0) {
+    if (KV == DSA_KV_FP8_E4M3 && tid < 128 && n_mine > 0) q_load(b, q0raw, q0w);
+    {
       // -inf (NaN for an over-long row) past the last valid page, split over
       // the row's G CTAs in contiguous 16-byte-aligned chunks
-      const bool bad = L > T;
+      fill_bad = L > T;
       const int f0 = npv * kPage;
       int chunk = (T - f0 + G - 1) / G;
       chunk = (chunk + 3) & ~3;
-      const long long beg = f0 + (long long)c * chunk;
-      const long long end = p.fill ? min(beg + chunk, (long long)T) : beg;
-      const float fv = bad ? nanf_() : -INFINITY;
-      const float4 v4 = make_float4(fv, fv, fv, fv);
-      const int nthr = n_mine == 0 ? kDecThreads : 128;
-      float* orow = p.out + (long long)b * p.out_stride;
-      for (long long i = beg + 4 * tid; i < end; i += 4 * nthr)
-        __stcs(reinterpret_cast<float4*>(orow + i), v4);
-      if (bad && c == 0 && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
+      fill_beg = f0 + (long long)c * chunk;
+      fill_end = p.fill ? min(fill_beg + chunk, (long long)T) : fill_beg;
+      if (fill_bad && c == 0 && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
     }
-    if (n_mine == 0) return;
+    if (n_mine == 0) {
+      const float fv = fill_bad ? nanf_() : -INFINITY;
+      const float4 v4 = make_float4(fv, fv, fv, fv);
+      float* orow = p.out + (long long)b * p.out_stride;
+      for (long long i = fill_beg + 4 * tid; i < fill_end; i += 4 * kDecThreads)
+        __stcs(reinterpret_cast<float4*>(orow + i), v4);
+      return;
+    }
     if (tid == 0) lens_s[0] = L;
+    my_pages = n_mine;
     tiles.init_request(G, c, b, n_mine);
   } else {
     // ---------------------------------------------------------------- balanced
@@ -339,61 +559,147 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         Pv[B] = run_v;
         Pf[B] = run_f;
       }
+      if (p.sel_k > 0) {
+        // fused top-k: exclusive prefix sums of the rows' chunk counts (the
+        // rows' first slots) replace the fill prefix sums
+        __syncwarp();
+        const Slicer sl(max(run_v, 1), gridDim.x);
+        int run_s = 0;
+        for (int base = 0; base < B; base += 32) {
+          const int j = base + lane;
+          const int cnt = j < B ? sl.row_chunks(Pv[j], Pv[j + 1], 1 << 30) : 0;
+          int sc = cnt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, sc, o);
+            if (lane >= o) sc += t;
+          }
+          if (j < B) Pf[j] = run_s + sc - cnt;
+          run_s += __shfl_sync(0xffffffffu, sc, 31);
+        }
+        if (lane == 0) Pf[B] = run_s;
+        __syncwarp();
+        if (blockIdx.x == 0) {
+          int* hdr = reinterpret_cast<int*>(p.sel_ws);
+          for (int j = lane; j <= B; j += 32) hdr[j] = Pf[j];
+        }
+      }
     }
     __syncthreads();
     const long long R = gridDim.x, k = blockIdx.x;
     const long long N = Pv[B], F = p.fill ? Pf[B] : 0;
     const int u0 = (int)(k * N / R), u1 = (int)((k + 1) * N / R);
     const int f0 = (int)(k * F / R), f1 = (int)((k + 1) * F / R);
+    if (u0 < u1) {
+      tiles.init_balanced(Pv, B, u0, u1);
+      if (KV == DSA_KV_FP8_E4M3 && tid < 128) q_load(tiles.row, q0raw, q0w);
+    }
 
-    // this CTA's share of the fill: fill pages [f0, f1) in row order; fill
-    // page i of row r is page valid_pages(L_r) + i of that row
-    if (f0 < f1 && (tid < 128 || u0 >= u1)) {
-      const int nthr = u0 >= u1 ? kDecThreads : 128;
-      int lo = 0, hi = B - 1;
-      while (lo < hi) {      // row holding fill page f0
-        const int mid = (lo + hi + 1) >> 1;
-        if (Pf[mid] <= f0) lo = mid; else hi = mid - 1;
-      }
-      for (int r = lo, f = f0; f < f1 && r < B; ++r) {
-        const int nf = Pf[r + 1] - Pf[r];
-        if (nf == 0) continue;
-        const int a = f - Pf[r];                       // first fill page of row r in range
-        const int e = min(f1 - Pf[r], nf);             // one past the last
-        const int L = lens_s[r];
-        const bool bad = L > T;
-        const int first_page = p.W - nf;               // = valid pages of row r
+    fill_f0 = f0;
+    fill_f1 = f1;
+    my_pages = u1 - u0;
+    if (u0 >= u1) {
+      // no pages: the whole CTA writes its share of the fill
+      for_each_fill_range(tid == 0, [&](float* dst, long long n, bool bad) {
         const float fv = bad ? nanf_() : -INFINITY;
         const float4 v4 = make_float4(fv, fv, fv, fv);
-        float* orow = p.out + (long long)r * p.out_stride;
-        const long long beg = (long long)(first_page + a) * kPage;
-        const long long end = (long long)(first_page + e) * kPage;
-        for (long long i = beg + 4 * tid; i < end; i += 4 * nthr)
-          __stcs(reinterpret_cast<float4*>(orow + i), v4);
-        if (bad && a == 0 && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
-        f = Pf[r] + e;
-      }
+        for (long long i = 4 * tid; i < n; i += 4 * kDecThreads)
+          __stcs(reinterpret_cast<float4*>(dst + i), v4);
+      });
+      return;
     }
-    if (u0 >= u1) return;
-    tiles.init_balanced(Pv, B, u0, u1);
   }
 
   if (warp == 5) {
     tmem_alloc(tmem_slot, 128);
     tmem_relinquish();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
+  // Barrier 2: the TMEM address (and, in per-request mode, the barrier
+  // initialisation) reaches the MMA and epilogue warps.  The producer only
+  // arrives: it uses neither, and starts loading pages at once.
+  if (warp == 4) {
+    asm volatile("bar.arrive 2, %0;" ::"n"(kDecThreads) : "memory");
+  } else {
+    tc_fence_before();
+    asm volatile("bar.sync 2, %0;" ::"n"(kDecThreads) : "memory");
+    tc_fence_after();
+  }
+  const uint32_t tmem_base = warp == 4 ? 0u : *tmem_slot;
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
+    // The fill goes out as bulk copies from blocks of -inf / NaN in shared
+    // memory, in step with the page loads: no thread stays busy writing it
+    // while the pages stream in.
+    const bool any_fill = balanced ? fill_f0 < fill_f1 : fill_end > fill_beg;
+    if (any_fill) {
+      const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      const float4 qnan = make_float4(nanf_(), nanf_(), nanf_(), nanf_());
+      for (int j = lane; j < kFillBlock / 16; j += 32) reinterpret_cast<float4*>(sInf)[j] = ninf;
+      for (int j = lane; j < kNanBlock / 16; j += 32) reinterpret_cast<float4*>(sNan)[j] = qnan;
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
     if (lane == 0) {
+      // A cursor over this CTA's share of the fill: the current range is
+      // f_n floats from f_dst (NaN for an over-long row); in balanced mode
+      // the next range starts at fill page f_fp, in row f_row or later.
+      float* f_dst = nullptr;
+      long long f_n = 0;
+      bool f_bad = false;
+      int f_row = 0, f_fp = fill_f0;
+      if (!balanced) {
+        f_dst = p.out + (long long)blockIdx.y * p.out_stride + fill_beg;
+        f_n = max(fill_end - fill_beg, 0ll);
+        f_bad = fill_bad;
+      } else if (fill_f0 < fill_f1) {
+        int lo = 0, hi = p.rows - 1;
+        while (lo < hi) {      // row holding fill page fill_f0
+          const int mid = (lo + hi + 1) >> 1;
+          if (Pf[mid] <= fill_f0) lo = mid; else hi = mid - 1;
+        }
+        f_row = lo;
+      }
+      auto next_range = [&]() -> bool {
+        if (!balanced || f_fp >= fill_f1) return false;
+        while (f_row < p.rows && Pf[f_row + 1] <= f_fp) ++f_row;
+        if (f_row >= p.rows) return false;
+        const int nf = Pf[f_row + 1] - Pf[f_row];
+        const int a = f_fp - Pf[f_row];                  // first fill page of the row in range
+        const int e = min(fill_f1 - Pf[f_row], nf);      // one past the last
+        f_bad = lens_s[f_row] > T;
+        if (f_bad && a == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
+        f_dst = p.out + (long long)f_row * p.out_stride + (long long)(p.W - nf + a) * kPage;
+        f_n = (long long)(e - a) * kPage;
+        f_fp = Pf[f_row] + e;
+        return true;
+      };
+      // issue `budget` more floats of the fill (a multiple of 4; < 0 = all)
+      auto issue_fill = [&](long long budget) {
+        bool any = false;
+        while (budget != 0) {
+          if (f_n == 0 && !next_range()) break;
+          long long n = min(f_n, (long long)((f_bad ? kNanBlock : kFillBlock) / 4));
+          if (budget > 0) n = min(n, budget);
+          bulk_store(f_dst, f_bad ? sNan : sInf, (uint32_t)(4 * n));
+          f_dst += n;
+          f_n -= n;
+          if (budget > 0) budget -= n;
+          any = true;
+        }
+        if (any) bulk_commit();
+      };
+      // the share per loaded page once the first S tiles are out
+      const long long fill_total = balanced ? (long long)(fill_f1 - fill_f0) * kPage
+                                            : max(fill_end - fill_beg, 0ll);
+      const long long paced_pages = max(my_pages - 2 * S, 1);
+      const long long per_page =
+          ((fill_total + paced_pages - 1) / paced_pages + kPage - 1) / kPage * kPage;
       Tiles it = tiles;
       int issued = 0, seg_loaded = -1;
       bool ok = true;
       for (int i = 0; it.valid(); ++i, it.next()) {
+        if (!kFillPaced && i == S) issue_fill(-1);
         if (KV == DSA_KV_BF16 && it.seg != seg_loaded) {
           // query of this row segment -> buffer seg % 2, once segment seg-2
           // (the buffer's previous user) has finished its MMAs
@@ -425,7 +731,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           const int pg = h == 0 ? it.pg0 : it.pg1;
           phys[h] = -1;
           if (pg >= 0) {
-            const int ph = __ldg(btrow + pg);
+            const int early = h == 0 ? pre_ph0 : pre_ph1;
+            const int ph = (i == 0 && !balanced) ? early : __ldg(btrow + pg);
             if (ph >= 0 && ph < p.num_pages) {
               phys[h] = ph;
               bytes += C::kPageBytes;
@@ -447,11 +754,14 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           }
         }
         issued = i + 1;
+        if (kFillPaced && i >= S - 1) issue_fill(per_page * (it.pg1 >= 0 ? 2 : 1));
       }
+      issue_fill(-1);                          // the rest of the fill
       if (!ok) {
         *abort_flag = 1;
         raise_status(p.status, DSA_ERR_TIMEOUT);
       }
+      bulk_wait_all();
       // never leave the CTA with copies in flight: wait for the last use of
       // every stage and query buffer (already complete on the normal path)
       for (int i = max(0, issued - S); i < issued; ++i)
@@ -527,61 +837,42 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     // + lo with a power-of-two scale per head (warp w owns heads 16w..16w+15,
     // lane l owns d = 4l..4l+3); both dtypes stage the head weights.
     auto prepare = [&](int r, int sb) {
-      float* ws = w_s + sb * kHeads;
       if (KV == DSA_KV_FP8_E4M3) {
-        const uint16_t* qrow = p.q + (long long)r * kHeads * kDim;
         uint2 qraw[16];
-#pragma unroll
-        for (int hh = 0; hh < 16; ++hh)
-          qraw[hh] = __ldg(reinterpret_cast<const uint2*>(qrow + (warp * 16 + hh) * kDim) + lane);
-        const float wv = lane < 16 ? __ldg(p.w + (long long)r * kHeads + warp * 16 + lane) : 0.f;
-        uint8_t* qb = sQ + sb * C::kQBytes;
-#pragma unroll
-        for (int hh = 0; hh < 16; ++hh) {
-          const int h = warp * 16 + hh;
-          float x[4] = {bf16f(qraw[hh].x & 0xffffu), bf16f(qraw[hh].x >> 16),
-                        bf16f(qraw[hh].y & 0xffffu), bf16f(qraw[hh].y >> 16)};
-          float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-          m = warp_max(m);
-          int e = 0;
-          if (m > 0.f) {
-            const int E = ((__float_as_int(m) >> 23) & 0xff) - 127;   // floor(log2 m), m normal
-            e = min(max(7 - E, -126), 126);
-          }
-          const float sc = exp2i(e);
-          uint32_t hi = 0, lo = 0;
-#pragma unroll
-          for (int j = 0; j < 4; j += 2) {
-            const float a0 = x[j] * sc, a1 = x[j + 1] * sc;
-            float h0, h1, l0, l1;
-            const uint32_t hc = to_e4m3x2(a0, a1, h0, h1);
-            const uint32_t lc = to_e4m3x2(a0 - h0, a1 - h1, l0, l1);
-            hi |= hc << (8 * j);
-            lo |= lc << (8 * j);
-          }
-          // row h, bytes [4*lane, 4*lane+4) of 128, 128-byte swizzle
-          const uint32_t off = h * 128 + ((((lane >> 2) ^ (h & 7)) << 4) | ((lane & 3) << 2));
-          *reinterpret_cast<uint32_t*>(qb + off) = hi;
-          *reinterpret_cast<uint32_t*>(qb + 8192 + off) = lo;
-          const float wh = __shfl_sync(0xffffffffu, wv, hh);
-          if (lane == 0) ws[h] = wh * exp2i(-e);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&qbar[sb]);
+        float wv;
+        q_load(r, qraw, wv);
+        q_convert(qraw, wv, sb);
       } else {
-        if (tid < kHeads) ws[tid] = __ldg(p.w + (long long)r * kHeads + tid);
+        if (tid < kHeads) w_s[sb * kHeads + tid] = __ldg(p.w + (long long)r * kHeads + tid);
       }
     };
 
     bool ok = true;
-    // segments 0 and 1 use fresh buffers
-    prepare(tiles.row, 0);
+    // segments 0 and 1 use fresh buffers; segment 0's query was loaded
+    // before the fill (fp8)
+    if (KV == DSA_KV_FP8_E4M3) q_convert(q0raw, q0w, 0);
+    else prepare(tiles.row, 0);
     const int r1 = tiles.next_segment_row();
     if (r1 >= 0) prepare(r1, 1);
     asm volatile("bar.sync 1, 128;" ::: "memory");
 
     const int r = warp * 32 + lane;            // accumulator row = TMEM lane
     const int half = r >> 6, slot = r & 63;
+    // fused top-k: the open chunk (row, first position, valid positions so
+    // far, its slot); chunk_row < 0 = none open
+    const bool sel = p.sel_k > 0 && balanced;   // the host launches it only so
+    float* selbuf = reinterpret_cast<float*>(sAux);
+    int* selhist = reinterpret_cast<int*>(sAux + kSelHist);
+    int* selscr = reinterpret_cast<int*>(sAux + kSelScratch);
+    int chunk_row = -1, chunk_seg = -1, chunk_c = -1, chunk_p0 = 0, chunk_n = 0, seg_first = 0;
+    int seg_slot0 = 0;                         // the segment's first slot
+    float* chunk_slot = nullptr;
+    auto flush_chunk = [&]() {
+      epi_sync();                              // every logit of the chunk is in selbuf
+      select_chunk(selbuf, chunk_n, chunk_p0, p.sel_k, chunk_slot, selhist, selscr);
+      epi_sync();                              // selbuf is free again
+      chunk_row = -1;
+    };
     Tiles it = tiles;
     int cur_seg = 0;
     for (int i = 0; it.valid(); ++i, it.next()) {
@@ -604,6 +895,31 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       const int row = it.row;
       const int L = balanced ? lens_s[row] : lens_s[0];
       const int Lc = L > T ? 0 : max(L, 0);
+      if (sel) {
+        // the tile's chunk: pages counted from the segment's first page, in
+        // groups of kSelChunkPages (tiles pair pages from the segment's
+        // first, so a tile never straddles two chunks)
+        const bool new_seg = it.seg != chunk_seg;
+        if (new_seg) seg_first = it.pg0;
+        const int c = (it.pg0 - seg_first) / kSelChunkPages;
+        if (chunk_row >= 0 && (new_seg || c != chunk_c)) flush_chunk();
+        if (new_seg) {
+          // slots of the row's chunks held by the CTAs before this one
+          const Slicer sl(max(Pv[p.rows], 1), gridDim.x);
+          seg_slot0 = Pf[row] + sl.row_chunks(Pv[row], Pv[row + 1], blockIdx.x);
+        }
+        if (chunk_row < 0) {
+          chunk_row = row;
+          chunk_seg = it.seg;
+          chunk_c = c;
+          chunk_p0 = (seg_first + c * kSelChunkPages) * kPage;
+          chunk_n = 0;
+          chunk_slot = p.sel_ws + sel_header_floats(p.rows) + (long long)(seg_slot0 + c) *
+                                                                sel_slot_floats(p.sel_k);
+        }
+        const int last_pg = it.pg1 >= 0 ? it.pg1 : it.pg0;
+        chunk_n = max(chunk_n, min((last_pg + 1) * kPage, Lc) - chunk_p0);
+      }
       const int pg = half ? it.pg1 : it.pg0;
       const bool row_valid = pg >= 0;
       const int t = pg * kPage + slot;
@@ -620,7 +936,11 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);   // warp-uniform for tcgen05.ld
       float* orow = p.out + (long long)row * p.out_stride;
       if (!ok) {
-        if (row_valid) orow[t] = t < Lc ? nanf_() : -INFINITY;
+        if (sel) {
+          if (row_valid && t < Lc) selbuf[t - chunk_p0] = nanf_();
+        } else if (row_valid) {
+          orow[t] = t < Lc ? nanf_() : -INFINITY;
+        }
         continue;
       }
       tc_fence_after();
@@ -660,9 +980,11 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         } else {
           o = scale * ((acc0.x + acc0.y) + (acc1.x + acc1.y));
         }
-        orow[t] = o;
+        if (!sel) orow[t] = o;
+        else if (t < Lc) selbuf[t - chunk_p0] = o;
       }
     }
+    if (sel && chunk_row >= 0) flush_chunk();
     if (!ok) raise_status(p.status, DSA_ERR_TIMEOUT);
   }
 
@@ -681,6 +1003,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 // the per-dtype cap and W; for a short table (W <= 64 pages, so no request is
 // long) about DSA_DEC_SMALL_PER_SM CTAs per SM in total, so that each CTA
 // pipelines a few pages instead of paying its start-up latency for one.
+bool decode_is_balanced(int W, int rows) { return W > 64 && rows <= kMaxRowsBalanced; }
+
 template <int KV>
 int decode_slots(int W, int B, int sms) {
   int G = W < DecCfg<KV>::kMaxSlots ? W : DecCfg<KV>::kMaxSlots;
@@ -689,9 +1013,10 @@ int decode_slots(int W, int B, int sms) {
   return G < 1 ? 1 : G;
 }
 
+// Per device: the shared-memory opt-in, the SM count and the CTAs the
+// balanced mode keeps resident (its grid), set up once.
 template <int KV>
-static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
-  // per device: the shared-memory opt-in, the SM count and the resident CTAs
+static cudaError_t decode_device_setup(int* dev_out, int* resident, int* sms) {
   static int resident_per_dev[kMaxDevices] = {0};
   static int sms_per_dev[kMaxDevices] = {0};
   constexpr int smem = dec_smem_bytes<KV>();
@@ -705,8 +1030,8 @@ static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
     e = cudaFuncSetAttribute(decode_kernel<KV>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    int sms = 0, smem_sm = 0;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    int n_sm = 0, smem_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
     if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
         cudaSuccess)
@@ -715,10 +1040,21 @@ static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
     // reserved per CTA) and the launch bounds
     int per_sm = smem_sm / (smem + 1024);
     if (per_sm > kCtasPerSm) per_sm = kCtasPerSm;
-    if (sms < 1) sms = 1;
-    resident_per_dev[dev] = sms * (per_sm > 0 ? per_sm : 1);
-    sms_per_dev[dev] = sms;
+    if (n_sm < 1) n_sm = 1;
+    resident_per_dev[dev] = n_sm * (per_sm > 0 ? per_sm : 1);
+    sms_per_dev[dev] = n_sm;
   }
+  *dev_out = dev;
+  *resident = resident_per_dev[dev];
+  *sms = sms_per_dev[dev];
+  return cudaSuccess;
+}
+
+template <int KV>
+static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
+  int dev = 0, resident = 0, sms = 0;
+  cudaError_t e = decode_device_setup<KV>(&dev, &resident, &sms);
+  if (e != cudaSuccess) return e;
   CUtensorMap kmap, qmap;
   if (!encode_kcache_map(&kmap, p)) return cudaErrorInvalidValue;
   if (KV == DSA_KV_BF16) {
@@ -726,12 +1062,12 @@ static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
   } else {
     memset(&qmap, 0, sizeof qmap);
   }
-  const int balanced = (p.W > 64 && p.rows <= kMaxRowsBalanced) ? 1 : 0;
-  const int G = decode_slots<KV>(p.W, p.rows, sms_per_dev[dev]);
+  const int balanced = decode_is_balanced(p.W, p.rows) ? 1 : 0;
+  const int G = decode_slots<KV>(p.W, p.rows, sms);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = balanced ? dim3(resident_per_dev[dev], 1) : dim3(G, p.rows);
+  cfg.gridDim = balanced ? dim3(resident, 1) : dim3(G, p.rows);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = dec_smem_bytes<KV>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -739,6 +1075,13 @@ static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_kernel<KV>, kmap, qmap, p, G, balanced);
+}
+
+// The balanced grid of the current device for keys of kv_dtype.
+cudaError_t decode_balanced_ctas(int kv_dtype, int* ctas) {
+  int dev = 0, sms = 0;
+  if (kv_dtype == DSA_KV_FP8_E4M3) return decode_device_setup<DSA_KV_FP8_E4M3>(&dev, ctas, &sms);
+  return decode_device_setup<DSA_KV_BF16>(&dev, ctas, &sms);
 }
 
 cudaError_t launch_decode(const RowsParams& p, cudaStream_t stream) {

@@ -5,13 +5,19 @@
 
 #include "dsa_common.cuh"
 #include "dsa_indexer.h"
+#include "topk_slots.cuh"
 
 namespace dsa {
 cudaError_t launch_decode(const RowsParams& p, cudaStream_t stream);
-cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream);
+cudaError_t launch_prefill(const RowsParams& p, const PrefillRequests& rq, cudaStream_t stream);
 cudaError_t launch_topk(const float* logits, long long ld, const int* seqlens, int rows, int T,
                         int k, int* idx, float* vals, long long out_stride, int* status,
                         cudaStream_t stream);
+cudaError_t launch_topk_merge(const float* ws, const int* seqlens, int rows, int T, int k,
+                              int* idx, float* vals, long long out_stride, int* status,
+                              cudaStream_t stream);
+bool decode_is_balanced(int W, int rows);
+cudaError_t decode_balanced_ctas(int kv_dtype, int* ctas);
 long long static_scratch_floats();
 cudaError_t static_scratch(float** ptr);
 cudaError_t launch_store(const uint16_t* k, const int* slots, int n, uint8_t* kcache,
@@ -69,6 +75,8 @@ int check_and_pack(const void* q, const float* w, const void* kcache,
   p->out_stride = out_stride;
   p->status = dev_status;
   p->fill = 1;
+  p->sel_k = 0;
+  p->sel_ws = nullptr;
   return DSA_OK;
 }
 
@@ -112,7 +120,9 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
   cudaError_t e;
   if (bt_stride == 0) {
     // one request's queries over one shared table: the query-tile kernel
-    e = dsa::launch_prefill(p, static_cast<cudaStream_t>(stream));
+    dsa::PrefillRequests one;
+    one.n_req = 0;
+    e = dsa::launch_prefill(p, one, static_cast<cudaStream_t>(stream));
   } else {
     // per-query table rows (several requests, multi-token decode): every
     // query token is a row of the decode kernel, with its own table row,
@@ -141,23 +151,86 @@ int dsa_indexer_logits_prefill_varlen(const void* q, const float* w, const void*
                           block_table, bt_stride, seqlens, n_q, H, D, page_size, W, out,
                           out_stride, dev_status, &p);
   if (st != DSA_OK) return st;
-  // one query-tile launch per request: its queries, lengths and output rows,
-  // over its own table row
-  for (int b = 0; b < n_req; ++b) {
-    const int a = cu_q[b], n = cu_q[b + 1] - cu_q[b];
-    if (n == 0) continue;
+  // the query-tile kernel over up to kMaxPrefillRequests requests per launch
+  // (one launch for most calls): each request's query tiles read its own
+  // table row
+  static_assert(sizeof(dsa::PrefillRequests) <= 2048, "request map fits the kernel parameters");
+  for (int b0 = 0; b0 < n_req; b0 += dsa::kMaxPrefillRequests) {
+    const int nb = n_req - b0 < dsa::kMaxPrefillRequests ? n_req - b0 : dsa::kMaxPrefillRequests;
+    const int a = cu_q[b0], rows = cu_q[b0 + nb] - a;
+    if (rows == 0) continue;
+    dsa::PrefillRequests rq;
+    rq.n_req = nb;
+    int tiles = 0;
+    for (int b = 0; b < nb; ++b) {
+      rq.tile0[b] = tiles;
+      rq.row0[b] = cu_q[b0 + b] - a;
+      tiles += (cu_q[b0 + b + 1] - cu_q[b0 + b] + 3) / 4;
+    }
+    rq.tile0[nb] = tiles;
+    rq.row0[nb] = rows;
     dsa::RowsParams pb = p;
     pb.q = p.q + (long long)a * dsa::kHeads * dsa::kDim;
     pb.w = p.w + (long long)a * dsa::kHeads;
     pb.seqlens = p.seqlens + a;
     pb.out = p.out + (long long)a * p.out_stride;
-    pb.block_table = p.block_table + (long long)b * bt_stride;
-    pb.bt_stride = 0;
-    pb.rows = n;
-    if (dsa::launch_prefill(pb, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    pb.block_table = p.block_table + (long long)b0 * bt_stride;
+    pb.bt_stride = bt_stride;
+    pb.rows = rows;
+    if (dsa::launch_prefill(pb, rq, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return DSA_ERR_CUDA;
   }
   return DSA_OK;
+}
+
+int dsa_indexer_topk_decode_form(const void* q, const float* w, const void* kcache,
+                                 const void* kscale, long long page_stride_bytes, int num_pages,
+                                 int kv_dtype, const int* block_table, long long bt_stride,
+                                 const int* seqlens, int B, int H, int D, int page_size, int W,
+                                 int k_top, int* topk_idx, float* topk_val, long long topk_stride,
+                                 float* workspace, long long workspace_floats, int* dev_status,
+                                 int form, void* stream) {
+  dsa::RowsParams p;
+  const long long T = (long long)W * dsa::kPage;
+  int st = check_and_pack(q, w, kcache, kscale, page_stride_bytes, num_pages, kv_dtype,
+                          block_table, bt_stride, seqlens, B, H, D, page_size, W, workspace, T,
+                          dev_status, &p);
+  if (st != DSA_OK) return st;
+  if (k_top < 1 || !topk_idx || topk_stride < k_top) return DSA_ERR_INVALID_ARG;
+  if (form != DSA_TOPK_AUTO && form != DSA_TOPK_TWO_PASS && form != DSA_TOPK_FUSED)
+    return DSA_ERR_INVALID_ARG;
+  if (B > 0 && workspace_floats < (long long)B * T) return DSA_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || (topk_val && !aligned(topk_val, 4))) return DSA_ERR_MISALIGNED;
+  if (B == 0) return DSA_OK;
+  if (B > 65535) return DSA_ERR_UNSUPPORTED;
+  p.fill = 0;      // the selection reads only t < L
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the fused form: the balanced decode, k small enough that a chunk keeps
+  // at most half of its positions, and the slots within the workspace
+  bool fused = false;
+  if (form != DSA_TOPK_TWO_PASS && k_top <= dsa::kSelMaxK && dsa::decode_is_balanced(W, B)) {
+    int ctas = 0;
+    if (dsa::decode_balanced_ctas(kv_dtype, &ctas) != cudaSuccess) return DSA_ERR_CUDA;
+    const long long slots = (long long)ctas + B + ((long long)B * W + dsa::kSelChunkPages - 1) /
+                                                       dsa::kSelChunkPages;
+    fused = dsa::sel_header_floats(B) + slots * dsa::sel_slot_floats(k_top) <= workspace_floats;
+  }
+  if (form == DSA_TOPK_FUSED && !fused) return DSA_ERR_UNSUPPORTED;
+  cudaError_t e;
+  if (fused) {
+    p.sel_k = k_top;
+    p.sel_ws = workspace;
+    e = dsa::launch_decode(p, s);
+    if (e == cudaSuccess)
+      e = dsa::launch_topk_merge(workspace, seqlens, B, (int)T, k_top, topk_idx, topk_val,
+                                 topk_stride, dev_status, s);
+  } else {
+    e = dsa::launch_decode(p, s);
+    if (e == cudaSuccess)
+      e = dsa::launch_topk(workspace, T, seqlens, B, (int)T, k_top, topk_idx, topk_val,
+                           topk_stride, dev_status, s);
+  }
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
@@ -167,24 +240,11 @@ int dsa_indexer_topk_decode(const void* q, const float* w, const void* kcache,
                             int k_top, int* topk_idx, float* topk_val, long long topk_stride,
                             float* workspace, long long workspace_floats, int* dev_status,
                             void* stream) {
-  dsa::RowsParams p;
-  const long long T = (long long)W * dsa::kPage;
-  int st = check_and_pack(q, w, kcache, kscale, page_stride_bytes, num_pages, kv_dtype,
-                          block_table, bt_stride, seqlens, B, H, D, page_size, W, workspace, T,
-                          dev_status, &p);
-  if (st != DSA_OK) return st;
-  if (k_top < 1 || !topk_idx || topk_stride < k_top) return DSA_ERR_INVALID_ARG;
-  if (B > 0 && workspace_floats < (long long)B * T) return DSA_ERR_INVALID_ARG;
-  if (!aligned(topk_idx, 4) || (topk_val && !aligned(topk_val, 4))) return DSA_ERR_MISALIGNED;
-  if (B == 0) return DSA_OK;
-  if (B > 65535) return DSA_ERR_UNSUPPORTED;
-  p.fill = 0;      // the selection reads only t < L
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = dsa::launch_decode(p, s);
-  if (e == cudaSuccess)
-    e = dsa::launch_topk(workspace, T, seqlens, B, (int)T, k_top, topk_idx, topk_val, topk_stride,
-                         dev_status, s);
-  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return dsa_indexer_topk_decode_form(q, w, kcache, kscale, page_stride_bytes, num_pages,
+                                      kv_dtype, block_table, bt_stride, seqlens, B, H, D,
+                                      page_size, W, k_top, topk_idx, topk_val, topk_stride,
+                                      workspace, workspace_floats, dev_status, DSA_TOPK_AUTO,
+                                      stream);
 }
 
 int dsa_indexer_topk_decode_static(const void* q, const float* w, const void* kcache,

@@ -33,6 +33,21 @@ struct RowsParams {
   int* status;                 // nullable
   int fill;                    // decode: 1 = write the -inf past each row's last valid
                                // page; 0 = leave it (top-k reads only t < L)
+  int sel_k;                   // decode, balanced mode: > 0 = fused top-k, each chunk's
+                               // sel_k best positions into the slots at sel_ws
+  float* sel_ws;               // the fused top-k's workspace (topk_slots.cuh)
+};
+
+// Prefill of several requests in one launch: request b's query rows are
+// rows row0[b] .. row0[b+1]-1 of the call, grouped into query tiles
+// tile0[b] .. tile0[b+1]-1 of four rows (the last one ragged), and read
+// the keys through block-table row b.  n_req = 0: one request, every row
+// reads table row 0.
+constexpr int kMaxPrefillRequests = 128;
+struct PrefillRequests {
+  int n_req;
+  int tile0[kMaxPrefillRequests + 1];
+  int row0[kMaxPrefillRequests + 1];
 };
 
 __device__ __forceinline__ void raise_status(int* status, int code) {

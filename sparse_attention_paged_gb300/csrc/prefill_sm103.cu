@@ -51,6 +51,7 @@ constexpr int kThreads = (kEpiWarps + 2) * 32;  // + TMA warp + MMA warp
 constexpr int kBox = kPage * 128;             // 8 KB: one page's 64 rows of 128 bytes
 constexpr int kBBytes = kN * kDim * 2;        // 64 KB: 2 x 256 rows x 128 B (bf16 K-blocks / e4m3 hi, lo)
 constexpr int kCtrl = 6144;
+constexpr int kCtrlReq = 4352;                // request map (tile0, row0) in the control block
 constexpr int kBtSmem = 4096;                 // block-table entries kept in shared memory
 constexpr long long kWaitLimit = 2000000000ll;   // ~1 s of SM clock: bound on any wait
 
@@ -97,11 +98,38 @@ __device__ __forceinline__ uint32_t to_e4m3x2(float a, float b, float& fa, float
   return (uint32_t)s;
 }
 
+// A query tile: up to kQT consecutive query rows of one request, and the
+// request's block-table row.
+struct QTile {
+  int row0;          // first query row
+  int n;             // rows in the tile (1..kQT)
+  const int* bt;     // the request's block-table row
+  int req;           // the request (0 for a one-request call)
+};
+
 struct Lens {
   int T;
   int nq;
   int nqt;
   const int* seqlens;
+  // several requests (n_req > 0): request b's query tiles are tiles
+  // tile0[b] .. tile0[b+1]-1 and its rows row0[b] .. row0[b+1]-1, its table
+  // row at bt + b * bt_stride; n_req = 0: one request, tile j = rows 4j..
+  int n_req;
+  const int* tile0;  // shared memory
+  const int* row0;   // shared memory
+  const int* bt;
+  long long bt_stride;
+  __device__ __forceinline__ QTile tile(int j) const {
+    if (n_req == 0) return {kQT * j, min(kQT, nq - kQT * j), bt, 0};
+    int lo = 0, hi = n_req - 1;          // the request holding tile j
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile0[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    const int r0 = row0[lo] + kQT * (j - tile0[lo]);
+    return {r0, min(kQT, row0[lo + 1] - r0), bt + (long long)lo * bt_stride, lo};
+  }
   // length of query i clamped to [0, T]; an over-long row counts as 0 here
   // (it is written NaN by the fill)
   __device__ __forceinline__ int valid(int i) const {
@@ -111,9 +139,10 @@ struct Lens {
   }
   // largest valid length among the queries of query tile j
   __device__ __forceinline__ int lmax(int j) const {
+    const QTile t = tile(j);
     int m = 0;
 #pragma unroll
-    for (int q = 0; q < kQT; ++q) m = max(m, valid(kQT * j + q));
+    for (int q = 0; q < kQT; ++q) m = max(m, q < t.n ? valid(t.row0 + q) : 0);
     return m;
   }
   __device__ __forceinline__ int tiles(int j) const { return (lmax(j) + kTileM - 1) / kTileM; }
@@ -149,7 +178,7 @@ struct ItemIter {
 template <int KV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                   const RowsParams p) {
+                   const RowsParams p, const __grid_constant__ PrefillRequests rq) {
   constexpr int kStages = PfCfg<KV>::kStages;
   constexpr int kABytes = PfCfg<KV>::kABytes;
   constexpr bool kFp8 = KV == DSA_KV_FP8_E4M3;
@@ -171,35 +200,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* scan = reinterpret_cast<int*>(ctrl + 2048);         // [kThreads]
   int* bt_s = reinterpret_cast<int*>(ctrl + kCtrl);        // [kBtSmem] the shared table row
   int* e_s = scan;                                          // fp8: [256] per-head exponents (after the split)
+  int* rq_tile0 = reinterpret_cast<int*>(ctrl + kCtrlReq);  // [kMaxPrefillRequests + 1]
+  int* rq_row0 = rq_tile0 + kMaxPrefillRequests + 1;        // [kMaxPrefillRequests + 1]
   static_assert((2 * kStages + 6) * 8 <= 256, "control block");
-  static_assert(2048 + kThreads * 4 <= kCtrl, "control block");
+  static_assert(2048 + kThreads * 4 <= kCtrlReq, "control block");
+  static_assert(kCtrlReq + 8 * (kMaxPrefillRequests + 1) <= kCtrl, "control block");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.W * kPage;
-  const int n_qt = (p.rows + kQT - 1) / kQT;
-  const Lens lens{T, p.rows, n_qt, p.seqlens};
+  const int n_qt = rq.n_req > 0 ? rq.tile0[rq.n_req] : (p.rows + kQT - 1) / kQT;
+  for (int b = tid; b <= rq.n_req; b += kThreads) {   // the request map, to shared memory
+    rq_tile0[b] = rq.tile0[b];
+    rq_row0[b] = rq.row0[b];
+  }
+  const Lens lens{T, p.rows, n_qt, p.seqlens, rq.n_req, rq_tile0, rq_row0, p.block_table,
+                  p.bt_stride};
   const int P = gridDim.x, k = blockIdx.x;
-  const int* bt = p.block_table;   // shared row (bt_stride == 0)
+  const bool shared_row = rq.n_req == 0;   // one request: every query reads table row 0
 
   // nothing above reads the call's inputs; from here on they may have been
   // written by the previous launch in the stream
   griddep_wait();
   griddep_launch_dependents();
 
-  // The one table row all queries share, staged in shared memory (its first
-  // kBtSmem entries): page ids are then read without a global round trip.
-  const int n_bt = min(p.W, kBtSmem);
-  for (int j = tid; j < n_bt; j += kThreads) bt_s[j] = __ldg(bt + j);
-  auto page_id = [&](int page) { return page < kBtSmem ? bt_s[page] : __ldg(bt + page); };
+  // Page ids come from shared memory: one request's table row (its first
+  // kBtSmem entries), or every request's row when they fit together (request
+  // b's at b * W); else from each tile's own row (L1-cached loads).
+  const bool all_rows = !shared_row && rq.n_req * p.W <= kBtSmem;
+  if (shared_row) {
+    for (int j = tid; j < min(p.W, kBtSmem); j += kThreads) bt_s[j] = __ldg(p.block_table + j);
+  } else if (all_rows) {
+    for (int j = tid; j < rq.n_req * p.W; j += kThreads) {
+      const int b = j / p.W, e = j - b * p.W;
+      bt_s[j] = __ldg(p.block_table + (long long)b * p.bt_stride + e);
+    }
+  }
+  __syncthreads();
+  auto page_id = [&](const QTile& tq, int page) {
+    if (shared_row) return page < kBtSmem ? bt_s[page] : __ldg(tq.bt + page);
+    return all_rows ? bt_s[tq.req * p.W + page] : __ldg(tq.bt + page);
+  };
 
   // ---- fill: rows of query tiles without any position tile (every length
   // <= 0, or over-long rows) are written here; the other tiles' tails are
   // written by the CTA that owns their first item.
   for (int j = k; j < n_qt; j += P) {
     if (lens.tiles(j) != 0) continue;
-    for (int q = 0; q < kQT; ++q) {
-      const int i = kQT * j + q;
-      if (i >= p.rows) break;
+    const QTile qt = lens.tile(j);
+    for (int q = 0; q < qt.n; ++q) {
+      const int i = qt.row0 + q;
       const bool bad = __ldg(p.seqlens + i) > T;
       const float fv = bad ? nanf_() : -INFINITY;
       float* orow = p.out + (long long)i * p.out_stride;
@@ -284,9 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ItemIter it;
     it.init(&lens, j_start, pt_start);
-    int nb = 0, issued = 0, cur_j = -1;
+    int nb = 0, issued = 0, cur_j = -1, tq_j = -1;
+    QTile tq = {0, 0, p.block_table, 0};
     bool ok = true;
     for (int i = 0; i < n_items; ++i, it.next()) {
+      if (it.j != tq_j) {             // the query tile's rows and table row
+        tq = lens.tile(it.j);
+        tq_j = it.j;
+      }
       if (!kFp8 && it.j != cur_j) {   // new query tile: reload B once the MMA is done with it
         if (lane == 0) {
           if (nb > 0) ok = mbar_wait_bounded(bempty, (nb - 1) & 1, kWaitLimit);
@@ -296,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane < 2)
-          tma_load_2d(sB + lane * (kBBytes / 2), &qmap, bfull, lane * kHalfRowUnits, it.j * kN);
+          tma_load_2d(sB + lane * (kBBytes / 2), &qmap, bfull, lane * kHalfRowUnits,
+                      tq.row0 * kHeads);
         cur_j = it.j;
         ++nb;
       }
@@ -312,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < PfCfg<KV>::kOps) {
         const int page = 2 * it.pt + (lane & 1);
         if (page * kPage < it.lmax) {     // a page some query of the tile needs
-          const int ph = page_id(page);
+          const int ph = page_id(tq, page);
           if (ph >= 0 && ph < p.num_pages) phys = ph;
         }
       }
@@ -405,10 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 128-byte swizzle; hi at +0, lo at +32 KB) with a power-of-two scale
     // 2^e per head (the head's largest |q| lands in [128, 256)), e in e_s.
     // Threads 2t and 2t+1 take row t, 64 values each.
-    auto split_queries = [&](int j) {
+    auto split_queries = [&](const QTile& tq) {
       const int row = tid >> 1, half = tid & 1;
-      const int qi = kQT * j + (row >> 6);
-      const bool live = qi < p.rows;
+      const int qi = tq.row0 + (row >> 6);
+      const bool live = (row >> 6) < tq.n;
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + ((long long)(live ? qi : 0) * kHeads + (row & 63)) * kDim + half * 64);
       // pass 1: the head's largest |q| (as float bits: non-negative floats
@@ -459,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ItemIter it;
     it.init(&lens, j_start, pt_start);
     int cur_j = -1;
+    QTile tqe = {0, 0, p.block_table, 0};
     int Lq = 0, Lmax = 0;
     float2 wreg[8];
 #pragma unroll
@@ -470,17 +526,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int a = i & 1;
       if (it.j != cur_j) {
         cur_j = it.j;
+        tqe = lens.tile(cur_j);
         if (kFp8) {
           // every thread is past its reads of the previous e_s; the MMA is
           // done with the previous B (its last accumulator has been read)
           asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
           if (nb > 0 && ok) ok = mbar_wait_bounded(bempty, (nb - 1) & 1, kWaitLimit);
           ++nb;
-          split_queries(cur_j);
+          split_queries(tqe);
           asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         }
-        const int qi = kQT * cur_j + qt;
-        if (qi < p.rows) {
+        const int qi = tqe.row0 + qt;
+        if (qt < tqe.n) {
           const float* wr = p.w + (long long)qi * kHeads + 2 * cq;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -491,16 +548,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        const int L = qi < p.rows ? __ldg(p.seqlens + qi) : 0;
+        const int L = qt < tqe.n ? __ldg(p.seqlens + qi) : 0;
         badq = L > T;
         Lq = badq ? 0 : max(L, 0);
         Lmax = it.lmax;
         // the tail of this query tile past its last position tile
         if (it.pt == 0) {
           const int f0 = it.ntl * kTileM;
-          for (int q = 0; q < kQT; ++q) {
-            const int qf = kQT * cur_j + q;
-            if (qf >= p.rows) break;
+          for (int q = 0; q < tqe.n; ++q) {
+            const int qf = tqe.row0 + q;
             const bool bad = __ldg(p.seqlens + qf) > T;
             const float fv = bad ? nanf_() : -INFINITY;
             float* orow = p.out + (long long)qf * p.out_stride;
@@ -516,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int phys = -1;
       float scale = 1.f;
       if (in_table && t < Lmax) {
-        phys = page_id(page);
+        phys = page_id(tqe, page);
         if (phys >= 0 && phys < p.num_pages && p.kscale != nullptr)
           scale = __ldg(reinterpret_cast<const float*>(p.kscale + (long long)phys * p.page_stride) +
                         slot);
@@ -563,8 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float k1 = (b0 ? part[3] : part[1]) + rb;
         res = (b1 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
       }
-      const int qi = kQT * cur_j + qt;
-      if (in_table && qi < p.rows) {
+      const int qi = tqe.row0 + qt;
+      if (in_table && qt < tqe.n) {
         float o;
         if (badq) {
           o = nanf_();
@@ -591,7 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int KV>
-static cudaError_t launch_prefill_t(const RowsParams& p, cudaStream_t stream) {
+static cudaError_t launch_prefill_t(const RowsParams& p, const PrefillRequests& rq,
+                                    cudaStream_t stream) {
   // per device: the shared-memory opt-in and the SM count (one CTA per SM)
   static int sms_per_dev[kMaxDevices] = {0};
   constexpr int smem = pf_smem_bytes<KV>();
@@ -627,12 +684,12 @@ static cudaError_t launch_prefill_t(const RowsParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel<KV>, kmap, qmap, p);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<KV>, kmap, qmap, p, rq);
 }
 
-cudaError_t launch_prefill(const RowsParams& p, cudaStream_t stream) {
-  if (p.kv_dtype == DSA_KV_FP8_E4M3) return launch_prefill_t<DSA_KV_FP8_E4M3>(p, stream);
-  return launch_prefill_t<DSA_KV_BF16>(p, stream);
+cudaError_t launch_prefill(const RowsParams& p, const PrefillRequests& rq, cudaStream_t stream) {
+  if (p.kv_dtype == DSA_KV_FP8_E4M3) return launch_prefill_t<DSA_KV_FP8_E4M3>(p, rq, stream);
+  return launch_prefill_t<DSA_KV_BF16>(p, rq, stream);
 }
 
 }  // namespace dsa

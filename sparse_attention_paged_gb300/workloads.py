@@ -353,6 +353,14 @@ def cfg4() -> Workload:
                              seed=0, kv_dtype=KV_BF16, poison_tail=False)
 
 
+def cfg4_small() -> Workload:
+    """Config 4's kernel at a size for detailed profiling: decode bf16, B=64,
+    W=512, L log-uniform 1024..32768 (a 537 MB pool; the call moves more
+    than L2 holds)."""
+    return decode_loguniform("decode_bf16_B64_W512", 64, 512, 1024, 32768, 512,
+                             seed=0, kv_dtype=KV_BF16, poison_tail=False)
+
+
 def cfg5() -> Workload:
     """Prefill bf16: 4,096 queries of one request, 352 pages (22,528
     positions), causal limit of query i = 18432 + i."""
@@ -428,14 +436,14 @@ def cfg8() -> StoreWorkload:
     return store_rows("store_fp8_n65536", 65536, 2048, seed=0)
 
 
-def cfg9() -> Workload:
-    """Config 3's decode call (fp8, B=64, W=4097) with top-2048 selection:
-    the positions and logits of each request's 2,048 best positions instead
-    of the [64, 262,208] logits."""
+def cfg9(k: int = 2048) -> Workload:
+    """Config 3's decode call (fp8, B=64, W=4097) with top-k selection (k =
+    2,048 by default): the positions and logits of each request's k best
+    positions instead of the [64, 262,208] logits."""
     w = cfg3(4097)
-    w.name = "decode_topk2048_fp8_B64_W4097"
+    w.name = f"decode_topk{k}_fp8_B64_W4097"
     w.kind = "topk"
-    w.meta["k_top"] = 2048
+    w.meta["k_top"] = k
     return w
 
 
@@ -472,10 +480,13 @@ NAMED = {
     "3short": lambda: [cfg3_short(4097)],
     "3short_capped": lambda: [cfg3_short(32)],
     "4": lambda: [cfg4()],
+    "4s": lambda: [cfg4_small()],
     "5": lambda: [cfg5()],
     "6": lambda: [cfg6()],
     "6v": lambda: [cfg6v()],
     "7": lambda: [cfg7()],
     "8": lambda: [cfg8()],
     "9": lambda: [cfg9()],
+    "9k256": lambda: [cfg9(256)],
+    "9k512": lambda: [cfg9(512)],
 }

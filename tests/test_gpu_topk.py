@@ -159,3 +159,116 @@ def test_topk_more_rows_than_pairs_of_sms(k):
     idx, val, st = _topk(w, k)
     assert st == 0
     _check(w, k, idx, val, list(range(w.R)))
+
+
+# --- the fused form (selection in the decode epilogue, then a merge) against
+# the two-pass form: the same positions and bit-identical logits ---------------
+
+def _fused_ws_floats(B, W, k):
+    import torch
+    ctas = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    hdr = (B + 1 + 3) // 4 * 4
+    return hdr + (ctas + B + (B * W + 31) // 32) * (4 + 2 * k)
+
+
+def _topk_form(w, k, form, ws_floats=None):
+    import torch
+    import sparse_attention_paged_gb300 as lib
+    dw = DeviceWorkload(w)
+    T = w.W * w.P
+    n = max(w.R * T, ws_floats or 0)
+    idx = torch.full((w.R, k), -7, dtype=torch.int32, device="cuda")
+    val = torch.full((w.R, k), 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.full((n,), 3.0, dtype=torch.float32, device="cuda")
+    st = lib.dsa_indexer_topk_decode_form(dw.q, dw.wt, dw.kcache, dw.kscale_ptr, w.page_stride,
+                                          w.num_pages, w.kv_dtype, dw.bt, w.bt_stride, dw.seqlens,
+                                          w.R, 64, 128, 64, w.W, k, idx, val, k, ws, n,
+                                          dw.status, form)
+    torch.cuda.synchronize()
+    return st, idx.cpu().numpy(), val.cpu().numpy(), int(dw.status.item())
+
+
+def _same_as_two_pass(w, k, expect_status=0):
+    import sparse_attention_paged_gb300 as lib
+    ws = _fused_ws_floats(w.R, w.W, k)
+    st2, i2, v2, s2 = _topk_form(w, k, lib.TOPK_TWO_PASS)
+    stf, i_f, v_f, sf = _topk_form(w, k, lib.TOPK_FUSED, ws)
+    assert st2 == 0 and stf == 0
+    assert s2 == expect_status and sf == expect_status
+    assert np.array_equal(i2, i_f)
+    assert np.array_equal(v2.view(np.uint32), v_f.view(np.uint32))
+    return i_f, v_f
+
+
+@pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
+@pytest.mark.parametrize("k", [1, 64, 300, 1024])
+def test_topk_fused_matches_two_pass(kv, k):
+    """Rows shorter than k, of exactly k, crossing several 2,048-position
+    chunks, and the whole table; a ragged last page."""
+    W = 150
+    T = W * 64
+    lens = [0, 1, 63, k, k + 1, 2047, 2048, 2049, 4100, 7000, T - 1, T]
+    w = wl.decode_with_lengths(f"tkf{k}", lens, W, seed=60 + k, kv_dtype=kv)
+    idx, val = _same_as_two_pass(w, k)
+    _check(w, k, idx, val, list(range(w.R)))
+
+
+def test_topk_fused_ties_bad_pages_and_long_rows():
+    """Tied logits (an all-zero query, zeroed pages), a page id outside the
+    pool (NaN logits, status 6) and an over-long row (status 7): both forms
+    agree bit for bit and report the same status."""
+    W, k = 120, 256
+    lens = [5000, 5000, 3000, 7680, 7681, 900]
+    w = wl.decode_with_lengths("tkf_ties", lens, W, seed=61)
+    w.q_bits[0] = 0
+    for pg in w.block_table[1, :20]:
+        base = int(pg) * w.page_stride
+        w.kcache[base: base + 8192] = 0
+    w.block_table = w.block_table.copy()
+    w.block_table[5, 3] = w.num_pages + 9
+    _same_as_two_pass(w, k, expect_status=7)
+
+
+def test_topk_fused_config3_batch():
+    import sparse_attention_paged_gb300 as lib
+    w = wl.cfg3(4097)
+    for k in (256, 1000):
+        idx, val = _same_as_two_pass(w, k)
+        L = w.seqlens
+        rows = sorted(set([int(np.argmin(L)), int(np.argmax(L)), 0, 1, 17, 63]))
+        _check(w, k, idx, val, rows)
+    # with the contract's workspace (B * W * 64 floats) the automatic form is
+    # the fused one for k = 256 and the two-pass one for k = 2,048
+    st, i_a, v_a, s = _topk_form(w, 256, lib.TOPK_AUTO)
+    st_f, i_f, v_f, _ = _topk_form(w, 256, lib.TOPK_FUSED)
+    assert st == 0 and st_f == 0 and s == 0
+    assert np.array_equal(i_a, i_f)
+
+
+def test_topk_fused_refused_where_it_does_not_apply():
+    import sparse_attention_paged_gb300 as lib
+    # a short table (W <= 64) decodes per request: no fused form
+    w = wl.decode_with_lengths("tkf_short", [100, 2000], 40, seed=62)
+    st, idx, _, _ = _topk_form(w, 64, lib.TOPK_FUSED, _fused_ws_floats(2, 40, 64))
+    assert st == 2 and (idx == -7).all()
+    # k above half a chunk
+    w = wl.decode_with_lengths("tkf_bigk", [100, 9000], 150, seed=63)
+    st, _, _, _ = _topk_form(w, 1025, lib.TOPK_FUSED, _fused_ws_floats(2, 150, 1025))
+    assert st == 2
+    # a workspace too small for the slots
+    st, _, _, _ = _topk_form(w, 512, lib.TOPK_FUSED)
+    assert st == 2
+    # an unknown form
+    st, _, _, _ = _topk_form(w, 64, 7)
+    assert st == 1
+
+
+def test_topk_fused_row_with_more_candidates_than_shared_memory():
+    """Two requests over a 1,700-page table: the CTAs' slices are a few pages
+    each, so every chunk keeps all of its positions and the long row's
+    candidates (about 100,000) exceed what the merge stages in shared memory;
+    it reads them in place instead."""
+    W, k = 1700, 1024
+    w = wl.decode_with_lengths("tkf_huge", [100000, 4000], W, seed=64)
+    idx, val = _same_as_two_pass(w, k)
+    _check(w, k, idx, val, [0, 1])

@@ -1,5 +1,6 @@
-"""GPU parity of the varlen prefill (a block-table row per request, one
-query-tile launch per request) through the C ABI, against the oracle.  The
+"""GPU parity of the varlen prefill (a block-table row per request; the
+query-tile kernel over up to 128 requests per launch) through the C ABI,
+against the oracle.  The
 oracle reads the workload's per-query rows (copies of each request's row);
 the call gets one row per request and the request offsets."""
 import numpy as np
@@ -78,3 +79,23 @@ def test_config6_through_request_rows_sampled():
     ref, st = oracle_rows(w, rows)
     assert st == 0
     compare(o[rows], ref)
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_E4M3])
+def test_varlen_more_requests_than_one_launch_takes(kv):
+    """131 requests: two launches (128 requests, then 3), with empty and
+    one-token requests on both sides of the boundary."""
+    g = np.random.default_rng(7)
+    reqs = []
+    for b in range(131):
+        n = int(g.integers(0, 7))
+        if b in (0, 127, 128, 130):
+            n = 0 if b in (0, 128) else 1
+        c = int(g.integers(max(n, 1), 260))
+        reqs.append((n, c))
+    w = wl.prefill_varlen("vl_many", reqs, seed=44, kv_dtype=kv)
+    dw = _run_varlen(w)
+    assert int(dw.status.item()) == 0
+    ref, st = oracle_rows(w)
+    assert st == 0
+    compare(dw.out.cpu().numpy(), ref)
