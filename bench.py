@@ -127,7 +127,9 @@ KERNEL_SOURCES = {   # each kernel's own source and the shared code it includes
            "tensor_maps.cuh")
     for kind in ("decode", "prefill", "store")
 }
-KERNEL_SOURCES["topk"] = KERNEL_SOURCES["decode"] + ("topk_sm103.cu",)   # decode, then selection
+KERNEL_SOURCES["decode"] += ("topk_slots.cuh",)
+# decode, then the selection (two passes) or the merge (fused)
+KERNEL_SOURCES["topk"] = KERNEL_SOURCES["decode"] + ("topk_sm103.cu", "topk_fused_sm103.cu")
 
 
 def kernel_source_hash(kernel: str | None = None):

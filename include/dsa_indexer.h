@@ -179,7 +179,7 @@ int dsa_indexer_logits_prefill_varlen(const void* q, const float* w, const void*
 
 /* How the top-k decode computes its selection (dsa_indexer_topk_decode_form). */
 typedef enum {
-  DSA_TOPK_AUTO = 0,      /* the fused form where it applies, else two passes */
+  DSA_TOPK_AUTO = 0,      /* the library's choice (today: two passes) */
   DSA_TOPK_TWO_PASS = 1,  /* the logits into the workspace, then a selection kernel */
   DSA_TOPK_FUSED = 2      /* selection in the decode epilogue, then a merge kernel */
 } dsa_topk_form_t;
@@ -195,7 +195,8 @@ typedef enum {
  * position order.  workspace: device fp32 buffer of at least
  * B * W * 64 entries (16-byte aligned), owned by the caller; no -inf fill
  * is written anywhere.  Two kernel launches on `stream`, in one of two
- * forms (the fused one where it applies):
+ * forms (this entry point takes the two-pass one; the caller chooses with
+ * dsa_indexer_topk_decode_form):
  *   two passes: the decode kernel writes the logits of the valid positions
  *     into the workspace, then the selection kernel (a cluster of two CTAs
  *     per request while 2 * B CTAs fit in one wave of one CTA per SM, else

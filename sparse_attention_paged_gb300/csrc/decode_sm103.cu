@@ -72,7 +72,7 @@ namespace {
 #define DSA_DEC_CTAS 2
 #endif
 #ifndef DSA_DEC_SMALL_PER_SM
-#define DSA_DEC_SMALL_PER_SM 1
+#define DSA_DEC_SMALL_PER_SM 2
 #endif
 constexpr int kDecThreads = 192;          // warps 0-3 epilogue, 4 TMA, 5 MMA
 constexpr int kCtasPerSm = DSA_DEC_CTAS;
@@ -274,10 +274,13 @@ __device__ __forceinline__ int epi_scan(int v, int* scr, int* total) {
 // p0 + i at i).  Writes its best min(k, n) -- largest logit first, lower
 // position first among equal logits -- into `slot` in position order, with
 // the count.  The k-th best key is found by radix selection, 8 bits a pass
-// over a 256-bin histogram.  Called by the 128 epilogue threads together.
+// over a 256-bin histogram (one atomic per distinct digit per warp); the
+// taken positions are then compacted in order, each warp over a contiguous
+// quarter of the chunk, its lanes on consecutive entries.  Called by the 128
+// epilogue threads together.
 __device__ void select_chunk(const float* buf, int n, int p0, int k, float* slot, int* hist,
                              int* scr) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   float* vals = slot + kSlotHead;
   int* poss = reinterpret_cast<int*>(slot + kSlotHead + k);
   if (n <= k) {
@@ -295,9 +298,16 @@ __device__ void select_chunk(const float* buf, int n, int p0, int k, float* slot
     hist[tid] = 0;
     hist[tid + 128] = 0;
     epi_sync();
-    for (int i = tid; i < n; i += 128) {
-      const uint32_t key = sel_key(buf[i]);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+    for (int base = 0; base < n; base += 128) {
+      const int i = base + tid;
+      const uint32_t key = i < n ? sel_key(buf[i]) : 0u;
+      const bool m = i < n && (key & mask) == prefix;
+      const unsigned act = __ballot_sync(0xffffffffu, m);
+      if (m) {
+        const uint32_t d = (key >> shift) & 255u;
+        const unsigned peers = __match_any_sync(act, d);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+      }
     }
     epi_sync();
     const int d1 = 255 - 2 * tid, d0 = d1 - 1;   // this thread's digits, high first
@@ -319,28 +329,43 @@ __device__ void select_chunk(const float* buf, int n, int p0, int k, float* slot
     epi_sync();                               // hist and scr[4..5] are reused
   }
   // prefix is the k-th best key; `need` keys equal to it are taken, the
-  // lowest positions first.  Thread t writes [16t, 16t + 16) in order.
-  const int i0 = 16 * tid, i1 = min(i0 + 16, n);
-  int gt = 0, eq = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = sel_key(buf[i]);
-    gt += key > prefix;
-    eq += key == prefix;
+  // lowest positions first.  Warp w compacts [b0, b1).
+  const int per = ((n + 3) / 4 + 31) & ~31;
+  const int b0 = min(w * per, n), b1 = min(b0 + per, n);
+  const unsigned lt = (1u << lane) - 1u;
+  int gt_w = 0, eq_w = 0;
+  for (int i0 = b0; i0 < b1; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < b1 ? sel_key(buf[i]) : 0u;
+    gt_w += __popc(__ballot_sync(0xffffffffu, i < b1 && key > prefix));
+    eq_w += __popc(__ballot_sync(0xffffffffu, i < b1 && key == prefix));
   }
-  int tot;
-  const int eq_before = epi_scan(eq, scr, &tot);
-  const int eq_take = min(max(need - eq_before, 0), eq);
-  int o = epi_scan(gt + eq_take, scr, &tot);
-  int e = eq_before;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = sel_key(buf[i]);
-    bool take = key > prefix;
-    if (key == prefix) take = e++ < need;
+  if (lane == 0) {
+    scr[8 + w] = gt_w;
+    scr[12 + w] = eq_w;
+  }
+  epi_sync();
+  int o = 0, e = 0;                           // taken, and equal keys, before this warp
+  for (int v = 0; v < w; ++v) {
+    const int eqv = scr[12 + v];
+    o += scr[8 + v] + min(max(need - e, 0), eqv);
+    e += eqv;
+  }
+  for (int i0 = b0; i0 < b1; i0 += 32) {
+    const int i = i0 + lane;
+    const float v = i < b1 ? buf[i] : 0.f;
+    const uint32_t key = sel_key(v);
+    const bool g = i < b1 && key > prefix, q = i < b1 && key == prefix;
+    const unsigned qb = __ballot_sync(0xffffffffu, q);
+    const bool take = g || (q && e + __popc(qb & lt) < need);
+    const unsigned tb = __ballot_sync(0xffffffffu, take);
     if (take) {
-      vals[o] = buf[i];
-      poss[o] = p0 + i;
-      ++o;
+      const int dst = o + __popc(tb & lt);
+      vals[dst] = v;
+      poss[dst] = p0 + i;
     }
+    o += __popc(tb);
+    e += __popc(qb);
   }
   if (tid == 0) *reinterpret_cast<int*>(slot) = k;
 }
@@ -447,7 +472,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     fence_proxy_async_smem();
     mbar_arrive(&qbar[sb]);
   };
-  uint2 q0raw[16];           // fp8: the first segment's query, loaded before the fill
+  uint2 q0raw[16];           // fp8: the first segment's query, loaded first of all
   float q0w = 0.f;
 
   // This CTA's share of the fill.  Per-request mode: floats [fill_beg,

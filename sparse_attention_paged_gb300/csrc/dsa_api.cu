@@ -205,10 +205,11 @@ int dsa_indexer_topk_decode_form(const void* q, const float* w, const void* kcac
   if (B > 65535) return DSA_ERR_UNSUPPORTED;
   p.fill = 0;      // the selection reads only t < L
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the fused form: the balanced decode, k small enough that a chunk keeps
-  // at most half of its positions, and the slots within the workspace
+  // the fused form (on request only: the two-pass form measured faster on
+  // every batch tried): the balanced decode, k small enough that a chunk
+  // keeps at most half of its positions, and the slots within the workspace
   bool fused = false;
-  if (form != DSA_TOPK_TWO_PASS && k_top <= dsa::kSelMaxK && dsa::decode_is_balanced(W, B)) {
+  if (form == DSA_TOPK_FUSED && k_top <= dsa::kSelMaxK && dsa::decode_is_balanced(W, B)) {
     int ctas = 0;
     if (dsa::decode_balanced_ctas(kv_dtype, &ctas) != cudaSuccess) return DSA_ERR_CUDA;
     const long long slots = (long long)ctas + B + ((long long)B * W + dsa::kSelChunkPages - 1) /

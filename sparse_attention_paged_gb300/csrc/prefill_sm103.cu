@@ -50,8 +50,25 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = (kEpiWarps + 2) * 32;  // + TMA warp + MMA warp
 constexpr int kBox = kPage * 128;             // 8 KB: one page's 64 rows of 128 bytes
 constexpr int kBBytes = kN * kDim * 2;        // 64 KB: 2 x 256 rows x 128 B (bf16 K-blocks / e4m3 hi, lo)
-constexpr int kCtrl = 6144;
+constexpr int kCtrl = 10240;
 constexpr int kCtrlReq = 4352;                // request map (tile0, row0) in the control block
+constexpr int kCtrlWScan = kCtrlReq + 8 * (kMaxPrefillRequests + 1);   // [kThreads] long long
+// The persistent split balances cost, not items: an item weighs 16, a query
+// tile adds a fixed kTileChangeW (its query tile's load, weights and set-up:
+// about two items) and 1/20 per 64-position page of its rows' tail, which
+// the epilogue writes with -inf when it starts the tile.  CTAs on tiles of
+// short contexts (frequent tile changes, long tails) so take fewer items.
+// (Weights chosen by measurement among 0..64 per tile and 0..2/5 per page.)
+#ifndef DSA_PF_TILE_W
+#define DSA_PF_TILE_W 32
+#endif
+#ifndef DSA_PF_FILL_W_NUM
+#define DSA_PF_FILL_W_NUM 1
+#endif
+#ifndef DSA_PF_FILL_W_DEN
+#define DSA_PF_FILL_W_DEN 20
+#endif
+constexpr long long kTileChangeW = DSA_PF_TILE_W;
 constexpr int kBtSmem = 4096;                 // block-table entries kept in shared memory
 constexpr long long kWaitLimit = 2000000000ll;   // ~1 s of SM clock: bound on any wait
 
@@ -204,7 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* rq_row0 = rq_tile0 + kMaxPrefillRequests + 1;        // [kMaxPrefillRequests + 1]
   static_assert((2 * kStages + 6) * 8 <= 256, "control block");
   static_assert(2048 + kThreads * 4 <= kCtrlReq, "control block");
-  static_assert(kCtrlReq + 8 * (kMaxPrefillRequests + 1) <= kCtrl, "control block");
+  static_assert(kCtrlWScan + 8 * kThreads <= kCtrl && kCtrlWScan % 8 == 0, "control block");
+  long long* wscan = reinterpret_cast<long long*>(ctrl + kCtrlWScan);   // [kThreads]
+  long long* sm_wtot = reinterpret_cast<long long*>(ctrl + 304);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.W * kPage;
@@ -258,27 +277,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ---- this CTA's slice of the item list
+  // ---- this CTA's slice of the item list: an equal share of the cost
+  auto tile_weight = [&](int j, int nt) -> long long {
+    if (nt == 0) return 0;
+    const long long tail = (long long)lens.tile(j).n * max(p.W - 2 * nt, 0);
+    return 16ll * nt + kTileChangeW + tail * DSA_PF_FILL_W_NUM / DSA_PF_FILL_W_DEN;
+  };
   {
     const int j0 = (int)((long long)tid * n_qt / kThreads);
     const int j1 = (int)((long long)(tid + 1) * n_qt / kThreads);
     int part = 0;
-    for (int j = j0; j < j1; ++j) part += lens.tiles(j);
+    long long wpart = 0;
+    for (int j = j0; j < j1; ++j) {
+      const int nt = lens.tiles(j);
+      part += nt;
+      wpart += tile_weight(j, nt);
+    }
     scan[tid] = part;
+    wscan[tid] = wpart;
     __syncthreads();
     if (tid == 0) {
       int run = 0;
+      long long wrun = 0;
       for (int i = 0; i < kThreads; ++i) {
         const int v = scan[i];
+        const long long wv = wscan[i];
         scan[i] = run;
+        wscan[i] = wrun;
         run += v;
+        wrun += wv;
       }
       sm_misc[0] = run;
       sm_misc[1] = -1;
+      sm_misc[6] = run;          // item bounds of this CTA (found below)
+      sm_misc[7] = run;
+      *sm_wtot = wrun;
     }
     __syncthreads();
-    const int total = sm_misc[0];
-    const int start = (int)((long long)k * total / P);
+    // this CTA's items: from the first item whose cost range starts at or
+    // after k * TW / P up to the next CTA's first
+    const long long TW = *sm_wtot;
+    for (int e = 0; e < 2; ++e) {
+      const long long x = (long long)(k + e) * TW / P;
+      if (wpart > 0 && x >= wscan[tid] && x < wscan[tid] + wpart) {
+        long long acc = wscan[tid];
+        int ia = scan[tid];
+        for (int j = j0; j < j1; ++j) {
+          const int nt = lens.tiles(j);
+          const long long wt = tile_weight(j, nt);
+          if (x < acc + wt) {
+            // item 0 covers [acc, acc + wt - 16 (nt - 1)), item pt > 0 the
+            // 16 units after its predecessor
+            const long long f = wt - 16ll * nt;
+            int pt = 0;
+            if (x > acc) pt = (int)min((long long)nt, max(1ll, (x - acc - f + 15) / 16));
+            sm_misc[6 + e] = ia + pt;
+            break;
+          }
+          acc += wt;
+          ia += nt;
+        }
+      }
+    }
+    __syncthreads();
+    const int start = sm_misc[6];
     if (part > 0 && start >= scan[tid] && start < scan[tid] + part) {
       int acc = scan[tid];
       for (int j = j0; j < j1; ++j) {
@@ -293,9 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
   }
-  const int total = sm_misc[0];
-  const int start = (int)((long long)k * total / P);
-  const int n_items = (int)((long long)(k + 1) * total / P) - start;
+  const int n_items = sm_misc[7] - sm_misc[6];
   if (n_items <= 0) return;
   const int j_start = sm_misc[1], pt_start = sm_misc[2];
 

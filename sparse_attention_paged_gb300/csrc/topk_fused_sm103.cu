@@ -70,12 +70,13 @@ __device__ __forceinline__ int mg_scan(int v, int* scr, int* total) {
 // The k best of the candidates i in [0, n) with ok(i), in position order,
 // their logits and positions read through val(i) / pos(i); m of them are
 // ok.  Written in that order to oidx / oval and padded with -1 / -inf to k.
-// Radix selection over 256-bin histograms, then two block scans place the
-// taken candidates.
+// Radix selection over 256-bin histograms (one atomic per distinct digit per
+// warp), then an ordered compaction: warp w over a contiguous 1/16 of the
+// candidates, its lanes on consecutive ones, offsets from warp votes.
 template <class Ok, class Val, class Pos>
 __device__ void merge_select(int n, int m, int k, Ok ok, Val val, Pos pos, int* oidx,
                              float* oval, int* hist, int* scr) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const bool all = m <= k;
   uint32_t prefix = 0, mask = 0;
   int need = min(k, m);                      // still to take among keys matching prefix
@@ -84,10 +85,17 @@ __device__ void merge_select(int n, int m, int k, Ok ok, Val val, Pos pos, int* 
       const int shift = 24 - 8 * pass;
       if (tid < 256) hist[tid] = 0;
       __syncthreads();
-      for (int i = tid; i < n; i += kMgThreads) {
-        if (!ok(i)) continue;
-        const uint32_t key = sel_key(val(i));
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+      for (int base = 0; base < n; base += kMgThreads) {
+        const int i = base + tid;
+        const bool in = i < n && ok(i);
+        const uint32_t key = in ? sel_key(val(i)) : 0u;
+        const bool mt = in && (key & mask) == prefix;
+        const unsigned act = __ballot_sync(0xffffffffu, mt);
+        if (mt) {
+          const uint32_t d = (key >> shift) & 255u;
+          const unsigned peers = __match_any_sync(act, d);
+          if (lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+        }
       }
       __syncthreads();
       const int d = 255 - tid;               // one digit per thread (the first 256), high first
@@ -105,33 +113,50 @@ __device__ void merge_select(int n, int m, int k, Ok ok, Val val, Pos pos, int* 
       __syncthreads();
     }
   }
-  // thread t owns candidates [i0, i1): counts, then places
-  const int per = (n + kMgThreads - 1) / kMgThreads;
-  const int i0 = min(tid * per, n), i1 = min(i0 + per, n);
-  int gt = 0, eq = 0;
-  for (int i = i0; i < i1; ++i) {
-    if (!ok(i)) continue;
-    const uint32_t key = sel_key(val(i));
-    if (all || key > prefix) ++gt;
-    else if (key == prefix) ++eq;
+  // warp w compacts [b0, b1) in order
+  const int per = ((n + kMgWarps - 1) / kMgWarps + 31) & ~31;
+  const int b0 = min(w * per, n), b1 = min(b0 + per, n);
+  const unsigned lt = (1u << lane) - 1u;
+  int gt_w = 0, eq_w = 0;
+  for (int i0 = b0; i0 < b1; i0 += 32) {
+    const int i = i0 + lane;
+    const bool in = i < b1 && ok(i);
+    const uint32_t key = in ? sel_key(val(i)) : 0u;
+    gt_w += __popc(__ballot_sync(0xffffffffu, in && (all || key > prefix)));
+    eq_w += __popc(__ballot_sync(0xffffffffu, in && !all && key == prefix));
   }
-  int tot;
-  const int eq_before = mg_scan(eq, scr, &tot);
-  const int eq_take = min(max(need - eq_before, 0), eq);
-  int o = mg_scan(gt + eq_take, scr, &tot);
-  const int taken = tot;
-  int e = eq_before;
-  for (int i = i0; i < i1; ++i) {
-    if (!ok(i)) continue;
-    const float v = val(i);
-    const uint32_t key = sel_key(v);
-    bool take = all || key > prefix;
-    if (!all && key == prefix) take = e++ < need;
-    if (take) {
-      oidx[o] = pos(i);
-      if (oval) oval[o] = v;
-      ++o;
+  if (lane == 0) {
+    scr[kMgWarps + 2 + w] = gt_w;
+    scr[2 * kMgWarps + 2 + w] = eq_w;
+  }
+  __syncthreads();
+  int o = 0, e = 0, taken = 0;
+  for (int v = 0, ee = 0; v < kMgWarps; ++v) {
+    const int eqv = scr[2 * kMgWarps + 2 + v];
+    const int tv = scr[kMgWarps + 2 + v] + min(max(need - ee, 0), eqv);
+    if (v < w) {
+      o += tv;
+      e += eqv;
     }
+    taken += tv;
+    ee += eqv;
+  }
+  for (int i0 = b0; i0 < b1; i0 += 32) {
+    const int i = i0 + lane;
+    const bool in = i < b1 && ok(i);
+    const float v = in ? val(i) : 0.f;
+    const uint32_t key = sel_key(v);
+    const bool g = in && (all || key > prefix), q = in && !all && key == prefix;
+    const unsigned qb = __ballot_sync(0xffffffffu, q);
+    const bool take = g || (q && e + __popc(qb & lt) < need);
+    const unsigned tb = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int dst = o + __popc(tb & lt);
+      oidx[dst] = pos(i);
+      if (oval) oval[dst] = v;
+    }
+    o += __popc(tb);
+    e += __popc(qb);
   }
   for (int j = taken + tid; j < k; j += kMgThreads) {
     oidx[j] = -1;
@@ -142,7 +167,7 @@ __device__ void merge_select(int n, int m, int k, Ok ok, Val val, Pos pos, int* 
 __global__ void __launch_bounds__(kMgThreads) topk_merge_kernel(const MergeParams p) {
   extern __shared__ uint8_t mg_smem[];
   __shared__ int hist[256];
-  __shared__ int scr[kMgWarps + 2];
+  __shared__ int scr[3 * kMgWarps + 2];
   __shared__ int slot_off[kMgMaxSlots + 1];
   float* s_val = reinterpret_cast<float*>(mg_smem);
   int* s_pos = reinterpret_cast<int*>(mg_smem + kMgCap * 4);

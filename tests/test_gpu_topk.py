@@ -237,12 +237,13 @@ def test_topk_fused_config3_batch():
         L = w.seqlens
         rows = sorted(set([int(np.argmin(L)), int(np.argmax(L)), 0, 1, 17, 63]))
         _check(w, k, idx, val, rows)
-    # with the contract's workspace (B * W * 64 floats) the automatic form is
-    # the fused one for k = 256 and the two-pass one for k = 2,048
+    # the contract's workspace (B * W * 64 floats) holds the fused form's
+    # slots at k = 256, and the automatic form returns the same selection
     st, i_a, v_a, s = _topk_form(w, 256, lib.TOPK_AUTO)
     st_f, i_f, v_f, _ = _topk_form(w, 256, lib.TOPK_FUSED)
     assert st == 0 and st_f == 0 and s == 0
     assert np.array_equal(i_a, i_f)
+    assert np.array_equal(v_a.view(np.uint32), v_f.view(np.uint32))
 
 
 def test_topk_fused_refused_where_it_does_not_apply():
