@@ -71,9 +71,6 @@ namespace {
 #ifndef DSA_DEC_CTAS
 #define DSA_DEC_CTAS 2
 #endif
-#ifndef DSA_DEC_SMALL_PER_SM
-#define DSA_DEC_SMALL_PER_SM 2
-#endif
 constexpr int kDecThreads = 192;          // warps 0-3 epilogue, 4 TMA, 5 MMA
 constexpr int kCtasPerSm = DSA_DEC_CTAS;
 #ifndef DSA_WAIT_LIMIT_CYCLES
@@ -117,20 +114,21 @@ constexpr int kCtrlBytes = kCtrlPf + 4 * (kMaxRowsBalanced + 1);
 // logits, a 256-bin histogram and scan scratch.
 constexpr int kFillBlock = 4096;
 constexpr int kNanBlock = 1024;
-// The fill's bulk copies go out in step with the page loads (a share after
-// each tile from the S-th on) rather than all at once, so that DRAM serves a
-// steady mix of reads and writes and no load waits behind the whole fill.
-constexpr bool kFillPaced = true;
 constexpr int kSelHist = kSelChunk * 4;            // byte offsets in the region
 constexpr int kSelScratch = kSelHist + 256 * 4;
 constexpr int kSelBytes = kSelScratch + 64;
-constexpr int kAuxBytes = kSelBytes > kFillBlock + kNanBlock ? kSelBytes : kFillBlock + kNanBlock;
+// The logits kernel needs the fill blocks; the fused top-k's kernel (SEL)
+// the chunk buffer.
+template <bool SEL>
+constexpr int aux_bytes() {
+  return SEL ? kSelBytes : kFillBlock + kNanBlock;
+}
 
-template <int KV>
+template <int KV, bool SEL>
 constexpr int dec_smem_bytes() {
   using C = DecCfg<KV>;
-  return 1024 /* alignment slack */ + 2 * C::kQBytes + C::kStages * C::kTileBytes + kAuxBytes +
-         kCtrlBytes;
+  return 1024 /* alignment slack */ + 2 * C::kQBytes + C::kStages * C::kTileBytes +
+         aux_bytes<SEL>() + kCtrlBytes;
 }
 
 __device__ __forceinline__ float nanf_() { return __int_as_float(0x7fc00000); }
@@ -372,7 +370,10 @@ __device__ void select_chunk(const float* buf, int n, int p0, int k, float* slot
 
 }  // namespace
 
-template <int KV>
+// SEL: the fused top-k's instance (the epilogue keeps each chunk's logits in
+// shared memory and selects its best; no fill).  The logits instance carries
+// none of that code.
+template <int KV, bool SEL>
 __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                   const RowsParams p, const int G, const int balanced) {
@@ -383,10 +384,10 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
                                              ~uintptr_t(1023));
   uint8_t* sQ = smem;                          // 2 x B operand (row segments alternate)
   uint8_t* sA = smem + 2 * C::kQBytes;         // A stages
-  uint8_t* sAux = sA + S * C::kTileBytes;    // [kAuxBytes]
+  uint8_t* sAux = sA + S * C::kTileBytes;    // [aux_bytes<SEL>()]
   uint8_t* sInf = sAux;                       // fill: [kFillBlock] -inf
   uint8_t* sNan = sAux + kFillBlock;          // fill: [kNanBlock] NaN
-  uint8_t* ctrl = sAux + kAuxBytes;
+  uint8_t* ctrl = sAux + aux_bytes<SEL>();
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;                 // [2] accumulator ready
@@ -395,6 +396,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   uint64_t* bempty = qbar + 2;                 // [2] query operand no longer read
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 260);
+  int* slice_s = reinterpret_cast<int*>(ctrl + 264);    // balanced: this CTA's [u0, u1)
+  volatile int* tiles_out = reinterpret_cast<volatile int*>(ctrl + 272);  // producer: tiles issued
   float* w_s = reinterpret_cast<float*>(ctrl + 512);     // [2][64]
   int* lens_s = reinterpret_cast<int*>(ctrl + kCtrlLens);
   int* Pv = reinterpret_cast<int*>(ctrl + kCtrlPv);
@@ -418,6 +421,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       mbar_init(&bempty[a], 1);
     }
     *abort_flag = 0;
+    *tiles_out = 0;
     fence_barrier_init();
     prefetch_tmap(&kmap);
     if (KV == DSA_KV_BF16) prefetch_tmap(&qmap);
@@ -514,17 +518,9 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   };
 
   Tiles tiles;
-  int pre_ph0 = -1, pre_ph1 = -1;     // producer: the first tile's page ids, if loaded early
   if (!balanced) {
     // ---------------------------------------------------------------- per-request
     const int b = blockIdx.y, c = blockIdx.x;
-    if (tid == 128) {
-      // issued before the length arrives, so that the two loads overlap;
-      // used only for pages below the length
-      const int* btrow = p.block_table + (long long)b * p.bt_stride;
-      pre_ph0 = __ldg(btrow + c);
-      if (c + G < p.W) pre_ph1 = __ldg(btrow + c + G);
-    }
     const int L = __ldg(p.seqlens + b);
     const int npv = valid_pages(L, p.W);
     const int n_mine = npv > c ? (npv - 1 - c) / G + 1 : 0;
@@ -540,6 +536,17 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       fill_end = p.fill ? min(fill_beg + chunk, (long long)T) : fill_beg;
       if (fill_bad && c == 0 && tid == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
     }
+    // per-request mode: the epilogue warps write the CTA's share with
+    // streaming stores (its share is small; measured faster here than the
+    // producer's bulk copies, whose set-up every one of the many CTAs pays)
+    if (n_mine > 0 && tid < 128) {
+      const float fv = fill_bad ? nanf_() : -INFINITY;
+      const float4 v4 = make_float4(fv, fv, fv, fv);
+      float* orow = p.out + (long long)b * p.out_stride;
+      for (long long i = fill_beg + 4 * tid; i < fill_end; i += 4 * 128)
+        __stcs(reinterpret_cast<float4*>(orow + i), v4);
+    }
+    if (n_mine > 0) fill_end = fill_beg;    // nothing left for the producer
     if (n_mine == 0) {
       const float fv = fill_bad ? nanf_() : -INFINITY;
       const float4 v4 = make_float4(fv, fv, fv, fv);
@@ -584,7 +591,55 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         Pv[B] = run_v;
         Pf[B] = run_f;
       }
-      if (p.sel_k > 0) {
+      __syncwarp();
+      // fp8 keys: this CTA's pages [u0, u1) balance pages plus a weight Y
+      // per row start (a row segment's query is loaded and split by the
+      // CTA itself), Y = min(8, pages per CTA / 3) so that short slices are
+      // not swamped by it; each CTA takes the units whose weighted starts
+      // fall in [k * NW / R, (k + 1) * NW / R), a row's first unit weighing
+      // 1 + Y.  bf16 keys (the query comes by TMA) and the fused top-k (its
+      // slots follow the plain split) take Y = 0, the plain split.
+      const long long Rg = gridDim.x;
+      const long long Y = (KV == DSA_KV_FP8_E4M3 && !SEL)
+                              ? min(8ll, (long long)run_v / Rg / 3) : 0ll;
+      int n_rows = 0;
+      for (int base = 0; base < B; base += 32) {
+        const int j = base + lane;
+        n_rows += __popc(__ballot_sync(0xffffffffu, j < B && Pv[j + 1] > Pv[j]));
+      }
+      const long long NW = run_v + Y * n_rows;
+      for (int e = 0; e < 2; ++e) {
+        const long long x = (blockIdx.x + e) * NW / Rg;
+        int u = run_v, nb = 0;
+        bool found = false;
+        for (int base = 0; base < B && !found; base += 32) {
+          const int j = base + lane;
+          const int len = j < B ? Pv[j + 1] - Pv[j] : 0;
+          const int ne = len > 0 ? 1 : 0;
+          int incl = ne;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+          }
+          const long long pw = Pv[min(j, B)] + Y * (nb + incl - ne);   // the row's weighted start
+          const bool here = ne && x < pw + len + Y;
+          const unsigned hb = __ballot_sync(0xffffffffu, here);
+          if (hb) {
+            const int src = __ffs(hb) - 1;
+            int uu = 0;
+            if (lane == src) {
+              const long long i = x <= pw ? 0 : max(1ll, x - pw - Y);
+              uu = Pv[j] + (int)min(i, (long long)len);
+            }
+            u = __shfl_sync(0xffffffffu, uu, src);
+            found = true;
+          }
+          nb += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) slice_s[e] = u;
+      }
+      if (SEL) {
         // fused top-k: exclusive prefix sums of the rows' chunk counts (the
         // rows' first slots) replace the fill prefix sums
         __syncwarp();
@@ -612,8 +667,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     }
     __syncthreads();
     const long long R = gridDim.x, k = blockIdx.x;
-    const long long N = Pv[B], F = p.fill ? Pf[B] : 0;
-    const int u0 = (int)(k * N / R), u1 = (int)((k + 1) * N / R);
+    const long long F = p.fill ? Pf[B] : 0;
+    const int u0 = slice_s[0], u1 = slice_s[1];
     const int f0 = (int)(k * F / R), f1 = (int)((k + 1) * F / R);
     if (u0 < u1) {
       tiles.init_balanced(Pv, B, u0, u1);
@@ -654,8 +709,11 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     // The fill goes out as bulk copies from blocks of -inf / NaN in shared
-    // memory, in step with the page loads: no thread stays busy writing it
-    // while the pages stream in.
+    // memory, issued by lanes 1-31 (copies from one thread complete one after
+    // another; from 31 they overlap) as soon as lane 0 has issued its first
+    // stages' page loads.  No thread of the page stream stays busy with it.
+    // (Pacing the lanes by lane 0's progress was slower: the lanes' polling,
+    // divergent within lane 0's warp, took issue slots from the page loop.)
     const bool any_fill = balanced ? fill_f0 < fill_f1 : fill_end > fill_beg;
     if (any_fill) {
       const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -665,66 +723,35 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       fence_proxy_async_smem();
       __syncwarp();
     }
-    if (lane == 0) {
-      // A cursor over this CTA's share of the fill: the current range is
-      // f_n floats from f_dst (NaN for an over-long row); in balanced mode
-      // the next range starts at fill page f_fp, in row f_row or later.
-      float* f_dst = nullptr;
-      long long f_n = 0;
-      bool f_bad = false;
-      int f_row = 0, f_fp = fill_f0;
-      if (!balanced) {
-        f_dst = p.out + (long long)blockIdx.y * p.out_stride + fill_beg;
-        f_n = max(fill_end - fill_beg, 0ll);
-        f_bad = fill_bad;
-      } else if (fill_f0 < fill_f1) {
-        int lo = 0, hi = p.rows - 1;
-        while (lo < hi) {      // row holding fill page fill_f0
-          const int mid = (lo + hi + 1) >> 1;
-          if (Pf[mid] <= fill_f0) lo = mid; else hi = mid - 1;
-        }
-        f_row = lo;
-      }
-      auto next_range = [&]() -> bool {
-        if (!balanced || f_fp >= fill_f1) return false;
-        while (f_row < p.rows && Pf[f_row + 1] <= f_fp) ++f_row;
-        if (f_row >= p.rows) return false;
-        const int nf = Pf[f_row + 1] - Pf[f_row];
-        const int a = f_fp - Pf[f_row];                  // first fill page of the row in range
-        const int e = min(fill_f1 - Pf[f_row], nf);      // one past the last
-        f_bad = lens_s[f_row] > T;
-        if (f_bad && a == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
-        f_dst = p.out + (long long)f_row * p.out_stride + (long long)(p.W - nf + a) * kPage;
-        f_n = (long long)(e - a) * kPage;
-        f_fp = Pf[f_row] + e;
-        return true;
-      };
-      // issue `budget` more floats of the fill (a multiple of 4; < 0 = all)
-      auto issue_fill = [&](long long budget) {
+    // the first stages: after them (or after all tiles, if fewer) the fill may go
+    const int n_tiles = max((my_pages + 1) / 2, 1);
+    const int first_fill = min(S, n_tiles);
+    if (lane != 0) {
+      if (any_fill) {
+        // wait (bounded: ~0.3 s) for lane 0's first stages, then issue this
+        // lane's chunks: chunk c of the CTA's share (4 KB, or 1 KB of NaN)
+        // goes to lane 1 + c % 31
+        for (int spin = 0; *tiles_out < first_fill && spin < (1 << 22); ++spin) __nanosleep(64);
+        int c = 0;
         bool any = false;
-        while (budget != 0) {
-          if (f_n == 0 && !next_range()) break;
-          long long n = min(f_n, (long long)((f_bad ? kNanBlock : kFillBlock) / 4));
-          if (budget > 0) n = min(n, budget);
-          bulk_store(f_dst, f_bad ? sNan : sInf, (uint32_t)(4 * n));
-          f_dst += n;
-          f_n -= n;
-          if (budget > 0) budget -= n;
-          any = true;
+        for_each_fill_range(lane == 1, [&](float* dst, long long n, bool bad) {
+          const long long blk = (bad ? kNanBlock : kFillBlock) / 4;
+          for (long long i = 0; i < n; i += blk, ++c) {
+            if (c % 31 != lane - 1) continue;
+            bulk_store(dst + i, bad ? sNan : sInf, (uint32_t)(4 * min(blk, n - i)));
+            any = true;
+          }
+        });
+        if (any) {
+          bulk_commit();
+          bulk_wait_reads();    // the fill blocks are read: the CTA may exit
         }
-        if (any) bulk_commit();
-      };
-      // the share per loaded page once the first S tiles are out
-      const long long fill_total = balanced ? (long long)(fill_f1 - fill_f0) * kPage
-                                            : max(fill_end - fill_beg, 0ll);
-      const long long paced_pages = max(my_pages - 2 * S, 1);
-      const long long per_page =
-          ((fill_total + paced_pages - 1) / paced_pages + kPage - 1) / kPage * kPage;
+      }
+    } else {
       Tiles it = tiles;
       int issued = 0, seg_loaded = -1;
       bool ok = true;
       for (int i = 0; it.valid(); ++i, it.next()) {
-        if (!kFillPaced && i == S) issue_fill(-1);
         if (KV == DSA_KV_BF16 && it.seg != seg_loaded) {
           // query of this row segment -> buffer seg % 2, once segment seg-2
           // (the buffer's previous user) has finished its MMAs
@@ -756,8 +783,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           const int pg = h == 0 ? it.pg0 : it.pg1;
           phys[h] = -1;
           if (pg >= 0) {
-            const int early = h == 0 ? pre_ph0 : pre_ph1;
-            const int ph = (i == 0 && !balanced) ? early : __ldg(btrow + pg);
+            const int ph = __ldg(btrow + pg);
             if (ph >= 0 && ph < p.num_pages) {
               phys[h] = ph;
               bytes += C::kPageBytes;
@@ -779,14 +805,13 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           }
         }
         issued = i + 1;
-        if (kFillPaced && i >= S - 1) issue_fill(per_page * (it.pg1 >= 0 ? 2 : 1));
+        *tiles_out = i + 1;
       }
-      issue_fill(-1);                          // the rest of the fill
+      *tiles_out = 1 << 30;                    // release the rest of the fill
       if (!ok) {
         *abort_flag = 1;
         raise_status(p.status, DSA_ERR_TIMEOUT);
       }
-      bulk_wait_all();
       // never leave the CTA with copies in flight: wait for the last use of
       // every stage and query buffer (already complete on the normal path)
       for (int i = max(0, issued - S); i < issued; ++i)
@@ -885,7 +910,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     const int half = r >> 6, slot = r & 63;
     // fused top-k: the open chunk (row, first position, valid positions so
     // far, its slot); chunk_row < 0 = none open
-    const bool sel = p.sel_k > 0 && balanced;   // the host launches it only so
+    const bool sel = SEL && balanced;          // the host launches it only so
     float* selbuf = reinterpret_cast<float*>(sAux);
     int* selhist = reinterpret_cast<int*>(sAux + kSelHist);
     int* selscr = reinterpret_cast<int*>(sAux + kSelScratch);
@@ -1024,35 +1049,43 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 // ----------------------------------------------------------------------------
 // host side
 
-// CTAs per request in per-request mode, from the launch shape only: at most
-// the per-dtype cap and W; for a short table (W <= 64 pages, so no request is
-// long) about DSA_DEC_SMALL_PER_SM CTAs per SM in total, so that each CTA
-// pipelines a few pages instead of paying its start-up latency for one.
 bool decode_is_balanced(int W, int rows) { return W > 64 && rows <= kMaxRowsBalanced; }
 
+// CTAs per request in per-request mode, from the launch shape only: at most
+// the per-dtype cap and W.  For a short table (W <= 64 pages, so no request
+// is long) about one CTA per SM in total: each CTA pipelines a few pages
+// instead of paying its start-up latency for one, and the next launch's
+// CTAs find room to start (programmatic dependent launch) while this one
+// runs.  Two per SM when a CTA would otherwise hold more than 8 pages.
+// (Measured: B=16/32 rows 5.5 us per launch at one per SM, 6.0 at two; 64
+// rows of 32 pages 8.6 us at two, 9.9 at one.)
 template <int KV>
 int decode_slots(int W, int B, int sms) {
   int G = W < DecCfg<KV>::kMaxSlots ? W : DecCfg<KV>::kMaxSlots;
-  const long long budget = (long long)sms * DSA_DEC_SMALL_PER_SM;
-  if (W <= 64 && (long long)B * G > budget) G = (int)(budget / B);
+  if (W <= 64) {
+    int g = sms / B > 1 ? sms / B : 1;
+    if ((W + g - 1) / g > 8) g = 2 * sms / B > 1 ? 2 * sms / B : 1;
+    if (G > g) G = g;
+  }
   return G < 1 ? 1 : G;
 }
 
 // Per device: the shared-memory opt-in, the SM count and the CTAs the
 // balanced mode keeps resident (its grid), set up once.
-template <int KV>
+template <int KV, bool SEL>
 static cudaError_t decode_device_setup(int* dev_out, int* resident, int* sms) {
   static int resident_per_dev[kMaxDevices] = {0};
   static int sms_per_dev[kMaxDevices] = {0};
-  constexpr int smem = dec_smem_bytes<KV>();
+  constexpr int smem = dec_smem_bytes<KV, SEL>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (sms_per_dev[dev] == 0) {
-    e = cudaFuncSetAttribute(decode_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(decode_kernel<KV, SEL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_kernel<KV>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(decode_kernel<KV, SEL>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int n_sm = 0, smem_sm = 0;
@@ -1075,10 +1108,10 @@ static cudaError_t decode_device_setup(int* dev_out, int* resident, int* sms) {
   return cudaSuccess;
 }
 
-template <int KV>
+template <int KV, bool SEL>
 static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
   int dev = 0, resident = 0, sms = 0;
-  cudaError_t e = decode_device_setup<KV>(&dev, &resident, &sms);
+  cudaError_t e = decode_device_setup<KV, SEL>(&dev, &resident, &sms);
   if (e != cudaSuccess) return e;
   CUtensorMap kmap, qmap;
   if (!encode_kcache_map(&kmap, p)) return cudaErrorInvalidValue;
@@ -1092,26 +1125,31 @@ static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = balanced ? dim3(resident, 1) : dim3(G, p.rows);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = dec_smem_bytes<KV>();
+  cfg.dynamicSmemBytes = dec_smem_bytes<KV, SEL>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<KV>, kmap, qmap, p, G, balanced);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<KV, SEL>, kmap, qmap, p, G, balanced);
 }
 
 // The balanced grid of the current device for keys of kv_dtype.
 cudaError_t decode_balanced_ctas(int kv_dtype, int* ctas) {
   int dev = 0, sms = 0;
-  if (kv_dtype == DSA_KV_FP8_E4M3) return decode_device_setup<DSA_KV_FP8_E4M3>(&dev, ctas, &sms);
-  return decode_device_setup<DSA_KV_BF16>(&dev, ctas, &sms);
+  if (kv_dtype == DSA_KV_FP8_E4M3)
+    return decode_device_setup<DSA_KV_FP8_E4M3, true>(&dev, ctas, &sms);
+  return decode_device_setup<DSA_KV_BF16, true>(&dev, ctas, &sms);
 }
 
 cudaError_t launch_decode(const RowsParams& p, cudaStream_t stream) {
-  if (p.kv_dtype == DSA_KV_FP8_E4M3) return launch_decode_t<DSA_KV_FP8_E4M3>(p, stream);
-  return launch_decode_t<DSA_KV_BF16>(p, stream);
+  if (p.sel_k > 0) {
+    if (p.kv_dtype == DSA_KV_FP8_E4M3) return launch_decode_t<DSA_KV_FP8_E4M3, true>(p, stream);
+    return launch_decode_t<DSA_KV_BF16, true>(p, stream);
+  }
+  if (p.kv_dtype == DSA_KV_FP8_E4M3) return launch_decode_t<DSA_KV_FP8_E4M3, false>(p, stream);
+  return launch_decode_t<DSA_KV_BF16, false>(p, stream);
 }
 
 }  // namespace dsa

@@ -114,9 +114,11 @@ __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// Wait until every bulk copy this thread committed has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+// Wait until every bulk copy this thread committed has read its shared-
+// memory source (the writes complete on their own; the grid's completion
+// orders them before later work).
+__device__ __forceinline__ void bulk_wait_reads() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // ---- tcgen05 ------------------------------------------------------------------
