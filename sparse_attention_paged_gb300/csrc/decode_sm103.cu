@@ -35,10 +35,11 @@
 //
 // fp8 keys are consumed as stored (e4m3, kind::f8f6f4).  The bf16 query is
 // split once per row segment into two e4m3 terms with a power-of-two scale
-// per head: q * 2^e_h = hi + lo, hi = e4m3(q * 2^e_h), lo = e4m3(q * 2^e_h -
-// hi), with 2^e_h folded into the head weight.  hi + lo reproduces every
-// bf16 value whose magnitude is at least ~2^-10 of its head's maximum
-// exactly, and the rest to within 2^-18 of the head's maximum.
+// per head: q * 2^e_h = hi + lo * 2^-5, hi = e4m3(q * 2^e_h), lo = e4m3((q *
+// 2^e_h - hi) * 2^5), with 2^e_h folded into the head weight.  The two terms
+// accumulate in TMEM apart (the lo term's 2^-5 is applied in the epilogue),
+// so hi + lo * 2^-5 reproduces every bf16 value whose magnitude is at least
+// ~2^-15 of its head's maximum exactly, and the rest to within 2^-22 of it.
 #include <cuda.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -140,7 +141,19 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // 2^e as a float, e in [-126, 127].
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
+
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// fp8 keys: the query's lo term is held times kLoScale, in a TMEM
+// accumulator of its own; TMEM columns of one CTA: two accumulator buffers
+// of 64 heads (bf16), each with a second one for the lo term (fp8)
+constexpr float kLoScale = 32.f;
+template <int KV>
+constexpr uint32_t dec_tmem_cols() { return KV == DSA_KV_FP8_E4M3 ? 256u : 128u; }
 
 // bf16 bits -> float (exact).
 __device__ __forceinline__ float bf16f(uint32_t bits) { return __uint_as_float(bits << 16); }
@@ -431,8 +444,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 
   // fp8 query split, done by warps 0-3 (warp w owns heads 16w..16w+15, lane
   // l owns d = 4l..4l+3): q_load fetches row r's query and head weights,
-  // q_convert writes q * 2^e_h = hi + lo into query buffer sb as two e4m3
-  // terms (K-major, 128-byte swizzle) and the weights w_h * 2^-e_h
+  // q_convert writes q * 2^e_h = hi + lo * 2^-5 into query buffer sb as two
+  // e4m3 terms (K-major, 128-byte swizzle) and the weights w_h * 2^-e_h
   auto q_load = [&](int r, uint2 (&raw)[16], float& wv) {
     const uint16_t* qrow = p.q + (long long)r * kHeads * kDim;
 #pragma unroll
@@ -462,7 +475,9 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         const float a0 = x[j] * sc, a1 = x[j + 1] * sc;
         float h0, h1, l0, l1;
         const uint32_t hc = to_e4m3x2(a0, a1, h0, h1);
-        const uint32_t lc = to_e4m3x2(a0 - h0, a1 - h1, l0, l1);
+        // the residual is exact in fp32 and below 2^3 (hi's half step for
+        // |a| < 2^8): times 2^5 it stays within e4m3's range
+        const uint32_t lc = to_e4m3x2((a0 - h0) * kLoScale, (a1 - h1) * kLoScale, l0, l1);
         hi |= hc << (8 * j);
         lo |= lc << (8 * j);
       }
@@ -691,7 +706,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   }
 
   if (warp == 5) {
-    tmem_alloc(tmem_slot, 128);
+    tmem_alloc(tmem_slot, dec_tmem_cols<KV>());
     tmem_relinquish();
   }
   // Barrier 2: the TMEM address (and, in per-request mode, the barrier
@@ -709,11 +724,17 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     // The fill goes out as bulk copies from blocks of -inf / NaN in shared
-    // memory, issued by lanes 1-31 (copies from one thread complete one after
-    // another; from 31 they overlap) as soon as lane 0 has issued its first
-    // stages' page loads.  No thread of the page stream stays busy with it.
-    // (Pacing the lanes by lane 0's progress was slower: the lanes' polling,
-    // divergent within lane 0's warp, took issue slots from the page loop.)
+    // memory.  Lanes 1-31 issue them all at once (copies from one thread
+    // complete one after another; from 31 they overlap) as soon as lane 0
+    // has issued its first stages' page loads.  bf16 keys, CTA with a long
+    // page stream (16 pages or more): lane 0 issues them instead, in step
+    // with its page loads, a share after every tile from the S-th on, so
+    // that DRAM serves a steady mix of reads and writes (measured ~1% faster
+    // on 2,048-page tables).  fp8 keys keep the burst alone: with the paced
+    // loop compiled in, their short calls were measured slower even where
+    // it never ran.  (Pacing lanes 1-31 by lane 0's progress, or the whole
+    // warp issuing the burst between lane 0's first and later stages, was
+    // also slower.)
     const bool any_fill = balanced ? fill_f0 < fill_f1 : fill_end > fill_beg;
     if (any_fill) {
       const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -726,8 +747,135 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     // the first stages: after them (or after all tiles, if fewer) the fill may go
     const int n_tiles = max((my_pages + 1) / 2, 1);
     const int first_fill = min(S, n_tiles);
+    constexpr bool kCanPace = KV == DSA_KV_BF16;
+    const bool paced = kCanPace && any_fill && my_pages >= 16;
+    const bool burst = any_fill && !paced;
+
+    // lane 0's share of the fill (paced): a cursor over the ranges, the
+    // current one f_n floats from f_dst (NaN for an over-long row), the next
+    // one starting at fill page f_fp in row f_row or later
+    float* f_dst = nullptr;
+    long long f_n = 0;
+    bool f_bad = false;
+    int f_row = 0, f_fp = fill_f0;
+    if (!balanced) {
+      f_dst = p.out + (long long)blockIdx.y * p.out_stride + fill_beg;
+      f_n = paced ? max(fill_end - fill_beg, 0ll) : 0;
+      f_bad = fill_bad;
+    } else if (paced && lane == 0) {
+      int lo = 0, hi = p.rows - 1;
+      while (lo < hi) {      // row holding fill page fill_f0
+        const int mid = (lo + hi + 1) >> 1;
+        if (Pf[mid] <= fill_f0) lo = mid; else hi = mid - 1;
+      }
+      f_row = lo;
+    } else {
+      f_fp = fill_f1;        // nothing for the cursor
+    }
+    auto next_range = [&]() -> bool {
+      if (!balanced || f_fp >= fill_f1) return false;
+      while (f_row < p.rows && Pf[f_row + 1] <= f_fp) ++f_row;
+      if (f_row >= p.rows) return false;
+      const int nf = Pf[f_row + 1] - Pf[f_row];
+      const int a = f_fp - Pf[f_row];                  // first fill page of the row in range
+      const int e = min(fill_f1 - Pf[f_row], nf);      // one past the last
+      f_bad = lens_s[f_row] > T;
+      if (f_bad && a == 0) raise_status(p.status, DSA_ERR_BAD_SEQLEN);
+      f_dst = p.out + (long long)f_row * p.out_stride + (long long)(p.W - nf + a) * kPage;
+      f_n = (long long)(e - a) * kPage;
+      f_fp = Pf[f_row] + e;
+      return true;
+    };
+    // issue `budget` more floats of lane 0's share (a multiple of 4; < 0 = all)
+    auto issue_fill = [&](long long budget) {
+      bool any = false;
+      while (budget != 0) {
+        if (f_n == 0 && !next_range()) break;
+        long long n = min(f_n, (long long)((f_bad ? kNanBlock : kFillBlock) / 4));
+        if (budget > 0) n = min(n, budget);
+        bulk_store(f_dst, f_bad ? sNan : sInf, (uint32_t)(4 * n));
+        f_dst += n;
+        f_n -= n;
+        if (budget > 0) budget -= n;
+        any = true;
+      }
+      if (any) bulk_commit();
+    };
+    // the paced share per loaded page, from the first stages on
+    long long per_page = 0;
+    if (paced) {
+      const long long fill_total =
+          balanced ? (long long)(fill_f1 - fill_f0) * kPage : max(fill_end - fill_beg, 0ll);
+      const long long paced_pages = max(my_pages - 2 * (first_fill - 1), 1);
+      per_page = ((fill_total + paced_pages - 1) / paced_pages + kPage - 1) / kPage * kPage;
+    }
+
+    // lane 0's page loop, compiled with and without the paced fill
+    int issued = 0, seg_loaded = -1;
+    bool ok = true;
+    auto page_loop = [&](auto paced_c) {
+      constexpr bool kPaced = decltype(paced_c)::value;
+      Tiles it = tiles;
+      for (int i = 0; it.valid(); ++i, it.next()) {
+          if (KV == DSA_KV_BF16 && it.seg != seg_loaded) {
+            // query of this row segment -> buffer seg % 2, once segment seg-2
+            // (the buffer's previous user) has finished its MMAs
+            const int sb = it.seg & 1;
+            if (it.seg >= 2) ok = mbar_wait_bounded(&bempty[sb], ((it.seg - 2) >> 1) & 1, kWaitLimit);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&qbar[sb], C::kQBytes);
+            tma_load_2d(sQ + sb * C::kQBytes, &qmap, &qbar[sb], 0, it.row * kHeads);
+            tma_load_2d(sQ + sb * C::kQBytes + C::kQBytes / 2, &qmap, &qbar[sb], kHalfRowUnits,
+                        it.row * kHeads);
+            seg_loaded = it.seg;
+          }
+          const int s = i % S;
+          if (i >= S) ok = mbar_wait_bounded(&empty[s], ((i / S) - 1) & 1, kWaitLimit);
+          if (!ok || *abort_flag) break;
+#ifdef DSA_TEST_SKIP_FIRST_TILE
+          // test builds only: never deliver the first tile, so that the MMA's
+          // bounded wait for it runs out and the call reports DSA_ERR_TIMEOUT
+          if (i == 0) {
+            issued = i + 1;
+            continue;
+          }
+#endif
+          const int* btrow = p.block_table + (long long)it.row * p.bt_stride;
+          int phys[2];
+          uint32_t bytes = 0;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int pg = h == 0 ? it.pg0 : it.pg1;
+            phys[h] = -1;
+            if (pg >= 0) {
+              const int ph = __ldg(btrow + pg);
+              if (ph >= 0 && ph < p.num_pages) {
+                phys[h] = ph;
+                bytes += C::kPageBytes;
+              }
+            }
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+          uint8_t* st = sA + s * C::kTileBytes;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (phys[h] < 0) continue;
+            if (KV == DSA_KV_FP8_E4M3) {
+              tma_load_3d(st + h * C::kPageBytes, &kmap, &full[s], 0, 0, phys[h]);
+            } else {
+              // K-block 0 (d 0..63) and K-block 1 (d 64..127), rows of 128 B
+              tma_load_3d(st + h * (C::kPageBytes / 2), &kmap, &full[s], 0, 0, phys[h]);
+              tma_load_3d(st + C::kTileBytes / 2 + h * (C::kPageBytes / 2), &kmap, &full[s],
+                          kHalfRowUnits, 0, phys[h]);
+            }
+          }
+          issued = i + 1;
+          *tiles_out = i + 1;
+          if (kPaced && i + 1 >= first_fill) issue_fill(per_page * (it.pg1 >= 0 ? 2 : 1));
+      }
+    };
     if (lane != 0) {
-      if (any_fill) {
+      if (burst) {
         // wait (bounded: ~0.3 s) for lane 0's first stages, then issue this
         // lane's chunks: chunk c of the CTA's share (4 KB, or 1 KB of NaN)
         // goes to lane 1 + c % 31
@@ -736,78 +884,19 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         bool any = false;
         for_each_fill_range(lane == 1, [&](float* dst, long long n, bool bad) {
           const long long blk = (bad ? kNanBlock : kFillBlock) / 4;
-          for (long long i = 0; i < n; i += blk, ++c) {
+          for (long long j = 0; j < n; j += blk, ++c) {
             if (c % 31 != lane - 1) continue;
-            bulk_store(dst + i, bad ? sNan : sInf, (uint32_t)(4 * min(blk, n - i)));
+            bulk_store(dst + j, bad ? sNan : sInf, (uint32_t)(4 * min(blk, n - j)));
             any = true;
           }
         });
-        if (any) {
-          bulk_commit();
-          bulk_wait_reads();    // the fill blocks are read: the CTA may exit
-        }
+        if (any) bulk_commit();
       }
     } else {
-      Tiles it = tiles;
-      int issued = 0, seg_loaded = -1;
-      bool ok = true;
-      for (int i = 0; it.valid(); ++i, it.next()) {
-        if (KV == DSA_KV_BF16 && it.seg != seg_loaded) {
-          // query of this row segment -> buffer seg % 2, once segment seg-2
-          // (the buffer's previous user) has finished its MMAs
-          const int sb = it.seg & 1;
-          if (it.seg >= 2) ok = mbar_wait_bounded(&bempty[sb], ((it.seg - 2) >> 1) & 1, kWaitLimit);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&qbar[sb], C::kQBytes);
-          tma_load_2d(sQ + sb * C::kQBytes, &qmap, &qbar[sb], 0, it.row * kHeads);
-          tma_load_2d(sQ + sb * C::kQBytes + C::kQBytes / 2, &qmap, &qbar[sb], kHalfRowUnits,
-                      it.row * kHeads);
-          seg_loaded = it.seg;
-        }
-        const int s = i % S;
-        if (i >= S) ok = mbar_wait_bounded(&empty[s], ((i / S) - 1) & 1, kWaitLimit);
-        if (!ok || *abort_flag) break;
-#ifdef DSA_TEST_SKIP_FIRST_TILE
-        // test builds only: never deliver the first tile, so that the MMA's
-        // bounded wait for it runs out and the call reports DSA_ERR_TIMEOUT
-        if (i == 0) {
-          issued = i + 1;
-          continue;
-        }
-#endif
-        const int* btrow = p.block_table + (long long)it.row * p.bt_stride;
-        int phys[2];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int pg = h == 0 ? it.pg0 : it.pg1;
-          phys[h] = -1;
-          if (pg >= 0) {
-            const int ph = __ldg(btrow + pg);
-            if (ph >= 0 && ph < p.num_pages) {
-              phys[h] = ph;
-              bytes += C::kPageBytes;
-            }
-          }
-        }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        uint8_t* st = sA + s * C::kTileBytes;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (phys[h] < 0) continue;
-          if (KV == DSA_KV_FP8_E4M3) {
-            tma_load_3d(st + h * C::kPageBytes, &kmap, &full[s], 0, 0, phys[h]);
-          } else {
-            // K-block 0 (d 0..63) and K-block 1 (d 64..127), rows of 128 B
-            tma_load_3d(st + h * (C::kPageBytes / 2), &kmap, &full[s], 0, 0, phys[h]);
-            tma_load_3d(st + C::kTileBytes / 2 + h * (C::kPageBytes / 2), &kmap, &full[s],
-                        kHalfRowUnits, 0, phys[h]);
-          }
-        }
-        issued = i + 1;
-        *tiles_out = i + 1;
-      }
-      *tiles_out = 1 << 30;                    // release the rest of the fill
+      if (kCanPace && paced) page_loop(BoolC<kCanPace>{});
+      else page_loop(BoolC<false>{});
+      *tiles_out = 1 << 30;                  // release the lanes' fill
+      if (paced) issue_fill(-1);             // the rest of lane 0's share
       if (!ok) {
         *abort_flag = 1;
         raise_status(p.status, DSA_ERR_TIMEOUT);
@@ -821,6 +910,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           mbar_wait_bounded(&qbar[sg & 1], (sg >> 1) & 1, kWaitLimit);
       }
     }
+    if (any_fill) bulk_wait_reads();         // the fill blocks are read: the CTA may exit
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -845,14 +935,15 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         const uint32_t st = sAa + s * C::kTileBytes;
         const uint32_t bq = sQa + (seg & 1) * C::kQBytes;
         if (KV == DSA_KV_FP8_E4M3) {
-          // A: 128 rows x 128 B; B: hi then lo, 64 rows x 128 B each; K = 32 per MMA
+          // A: 128 rows x 128 B; B: hi then lo, 64 rows x 128 B each; K = 32
+          // per MMA; the lo term into its own accumulator, 128 columns on
 #pragma unroll
           for (int term = 0; term < 2; ++term) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint64_t ad = smem_desc_sw128(st + 32 * k, 1024);
               const uint64_t bd = smem_desc_sw128(bq + term * 8192 + 32 * k, 1024);
-              mma_f8f6f4(d, ad, bd, idesc, (term | k) != 0);
+              mma_f8f6f4(d + term * 128, ad, bd, idesc, k != 0);
             }
           }
         } else {
@@ -994,15 +1085,48 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         continue;
       }
       tc_fence_after();
-      uint32_t v0[32], v1[32];
+      const float* ws = w_s + (cur_seg & 1) * kHeads;
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + a * kHeads;
+      if (KV == DSA_KV_FP8_E4M3) {
+        // S = hi + lo * 2^-5, 16 heads at a time (heads 0-31 to one partial
+        // sum, 32-63 to the other, as below); the next 16 heads' loads are
+        // in flight while the current ones are summed
+        uint32_t vh[2][16], vl[2][16];
+        tmem_ld_32x32b_x16(taddr, vh[0]);
+        tmem_ld_32x32b_x16(taddr + 128, vl[0]);
+        tmem_ld_wait(vh[0], vl[0]);
+        const float2 lsc = make_float2(1.f / kLoScale, 1.f / kLoScale);
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+          const int cb = part & 1;
+          if (part < 3) {
+            tmem_ld_32x32b_x16(taddr + 16 * (part + 1), vh[cb ^ 1]);
+            tmem_ld_32x32b_x16(taddr + 128 + 16 * (part + 1), vl[cb ^ 1]);
+          }
+          float2& acc = part < 2 ? acc0 : acc1;
+#pragma unroll
+          for (int h = 0; h < 16; h += 2) {
+            const float2 wv = *reinterpret_cast<const float2*>(ws + 16 * part + h);
+            const float2 sv = __ffma2_rn(
+                make_float2(__uint_as_float(vl[cb][h]), __uint_as_float(vl[cb][h + 1])), lsc,
+                make_float2(__uint_as_float(vh[cb][h]), __uint_as_float(vh[cb][h + 1])));
+            acc = __ffma2_rn(wv, make_float2(fmaxf(sv.x, 0.f), fmaxf(sv.y, 0.f)), acc);
+          }
+          if (part < 3) tmem_ld_wait(vh[cb ^ 1], vl[cb ^ 1]);
+          if (part == 2) {
+            // every column is in registers: the accumulator buffer is free
+            tc_fence_before();
+            mbar_arrive(&tempty[a]);
+          }
+        }
+      } else {
+      uint32_t v0[32], v1[32];
       tmem_ld_32x32b_x32(taddr, v0);
       tmem_ld_32x32b_x32(taddr + 32, v1);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&tempty[a]);
-      const float* ws = w_s + (cur_seg & 1) * kHeads;
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 32; h += 4) {
         const float4 wa = *reinterpret_cast<const float4*>(ws + h);
@@ -1019,6 +1143,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         acc1 = __ffma2_rn(make_float2(wb.z, wb.w),
                           make_float2(fmaxf(__uint_as_float(v1[h + 2]), 0.f),
                                       fmaxf(__uint_as_float(v1[h + 3]), 0.f)), acc1);
+      }
       }
       if (row_valid) {
         float o;
@@ -1042,7 +1167,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 128);
+    tmem_dealloc(tmem_base, dec_tmem_cols<KV>());
   }
 }
 

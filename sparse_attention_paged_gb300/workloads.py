@@ -174,6 +174,15 @@ def wide_range_queries(R: int, seed: int, outlier_d: int | None = None) -> np.nd
     return _bf16_bits(x.float())
 
 
+def zero_key_dim(w: "Workload", d: int) -> None:
+    """Set element d of every key in w's pool to zero (in place)."""
+    pool = w.kcache.reshape(w.num_pages, w.page_stride)
+    if w.kv_dtype == KV_E4M3:
+        pool[:, :FP8_SCALE_OFFSET].reshape(w.num_pages, P, D)[:, :, d] = 0
+    else:
+        pool.view(np.uint16).reshape(w.num_pages, P, D)[:, :, d] = 0
+
+
 def _used_pages(bt: np.ndarray, seqlens: np.ndarray, bt_stride: int) -> np.ndarray:
     used = []
     for r in range(len(seqlens)):

@@ -391,6 +391,19 @@ def test_decode_fp8_wide_range_queries(seed):
         assert stats["rel"] < 1e-3
 
 
+def test_decode_fp8_outliers_meet_zero_keys():
+    """Every head's outlier element sits at d = 5, where every key is zero,
+    so the dots come from the heads' small elements alone: the inputs on
+    which a query split with few bits below the head's largest element
+    misses the bar (test_fp8_split_host shows one that does)."""
+    for w in (wl.decode_uniform("wr_z", 16, 32, 2048, 512, seed=47),
+              wl.decode_with_lengths("wrl_z", [1, 64, 3000, 90 * 64], 90, seed=48)):
+        w.q_bits = wl.wide_range_queries(w.R, seed=54, outlier_d=5)
+        wl.zero_key_dim(w, 5)
+        stats = _check_full(w)
+        assert stats["rel"] < 1e-4
+
+
 def test_prefill_fp8_wide_range_queries():
     w = wl.prefill_causal("pf_wr", 130, 10, 10 * 64 - 140, seed=43, kv_dtype=wl.KV_E4M3)
     w.q_bits = wl.wide_range_queries(w.R, seed=52)
