@@ -644,31 +644,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + a * kN + qt * kHeads;
         float part[4];      // this thread's 16 heads of rows g, g+8, g+16, g+24
+        // four quarters (lane half x repeats 0-3 / 4-7), each load in flight
+        // while the quarter before it is summed
+        uint32_t v[2][16];
+        tmem_ld_16x256b_x4(taddr, v[0]);
+        tmem_ld_wait(v[0]);
+        float2 f0 = make_float2(0.f, 0.f), f1 = f0, s0 = f0, s1 = f0;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32];
-          tmem_ld_16x256b_x8(taddr + ((uint32_t)(16 * half) << 16), v);
-          tmem_ld_wait();
-          if (half == 1) {
+        for (int qr = 0; qr < 4; ++qr) {
+          const int half = qr >> 1, rep0 = (qr & 1) * 4, cb = qr & 1;
+          if (qr < 3) {
+            const int nh = (qr + 1) >> 1, nr = ((qr + 1) & 1) * 4;
+            tmem_ld_16x256b_x4(taddr + ((uint32_t)(16 * nh) << 16) + 8 * nr, v[cb ^ 1]);
+          }
+          // ReLU split over two pipes: even repeats by fmax (ALU pipe), odd
+          // ones by sat(s * 2^-64) (FMA pipe) in their own sums, scaled back
+          // by 2^64.
+#pragma unroll
+          for (int j = 0; j < 4; j += 2) {
+            const uint32_t* u = v[cb];
+            f0 = __ffma2_rn(wreg[rep0 + j], make_float2(fmaxf(__uint_as_float(u[4 * j]), 0.f),
+                                                        fmaxf(__uint_as_float(u[4 * j + 1]), 0.f)), f0);
+            f1 = __ffma2_rn(wreg[rep0 + j], make_float2(fmaxf(__uint_as_float(u[4 * j + 2]), 0.f),
+                                                        fmaxf(__uint_as_float(u[4 * j + 3]), 0.f)), f1);
+            s0 = __ffma2_rn(wreg[rep0 + j + 1], make_float2(relu_sat(__uint_as_float(u[4 * j + 4])),
+                                                            relu_sat(__uint_as_float(u[4 * j + 5]))), s0);
+            s1 = __ffma2_rn(wreg[rep0 + j + 1], make_float2(relu_sat(__uint_as_float(u[4 * j + 6])),
+                                                            relu_sat(__uint_as_float(u[4 * j + 7]))), s1);
+          }
+          if (qr < 3) tmem_ld_wait(v[cb ^ 1]);
+          if (qr == 2) {
+            // every column is in registers: the accumulator buffer is free
             tc_fence_before();
             mbar_arrive(&tempty[a]);
           }
-          // ReLU split over two pipes: even j by fmax (ALU pipe), odd j by
-          // sat(s * 2^-64) (FMA pipe) in their own sums, scaled back by 2^64.
-          float2 f0 = make_float2(0.f, 0.f), f1 = f0, s0 = f0, s1 = f0;
-#pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            f0 = __ffma2_rn(wreg[j], make_float2(fmaxf(__uint_as_float(v[4 * j]), 0.f),
-                                                 fmaxf(__uint_as_float(v[4 * j + 1]), 0.f)), f0);
-            f1 = __ffma2_rn(wreg[j], make_float2(fmaxf(__uint_as_float(v[4 * j + 2]), 0.f),
-                                                 fmaxf(__uint_as_float(v[4 * j + 3]), 0.f)), f1);
-            s0 = __ffma2_rn(wreg[j + 1], make_float2(relu_sat(__uint_as_float(v[4 * j + 4])),
-                                                     relu_sat(__uint_as_float(v[4 * j + 5]))), s0);
-            s1 = __ffma2_rn(wreg[j + 1], make_float2(relu_sat(__uint_as_float(v[4 * j + 6])),
-                                                     relu_sat(__uint_as_float(v[4 * j + 7]))), s1);
+          if (qr & 1) {
+            part[2 * half] = (f0.x + f0.y) + kTwo64 * (s0.x + s0.y);
+            part[2 * half + 1] = (f1.x + f1.y) + kTwo64 * (s1.x + s1.y);
+            f0 = f1 = s0 = s1 = make_float2(0.f, 0.f);
           }
-          part[2 * half] = (f0.x + f0.y) + kTwo64 * (s0.x + s0.y);
-          part[2 * half + 1] = (f1.x + f1.y) + kTwo64 * (s1.x + s1.y);
         }
         // reduce-scatter over c: bit 0 picks rows {g+16, g+24} or {g, g+8},
         // bit 1 the second or first of the pair
