@@ -39,7 +39,7 @@
 // 2^e_h - hi) * 2^5), with 2^e_h folded into the head weight.  The two terms
 // accumulate in TMEM apart (the lo term's 2^-5 is applied in the epilogue),
 // so hi + lo * 2^-5 reproduces every bf16 value whose magnitude is at least
-// ~2^-15 of its head's maximum exactly, and the rest to within 2^-22 of it.
+// 2^-14 of its head's maximum exactly, and the rest to within 2^-22 of it.
 #include <cuda.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
