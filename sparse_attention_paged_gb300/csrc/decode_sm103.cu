@@ -389,7 +389,7 @@ __device__ void select_chunk(const float* buf, int n, int p0, int k, float* slot
 template <int KV, bool SEL>
 __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                  const RowsParams p, const int G, const int balanced) {
+                  const RowsParams p, const int G, const int balanced, const int early_tmem) {
   using C = DecCfg<KV>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -439,6 +439,24 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     prefetch_tmap(&kmap);
     if (KV == DSA_KV_BF16) prefetch_tmap(&qmap);
   }
+  // With more than one CTA per SM, the tensor memory is taken before the
+  // wait for the previous launch: an SM was measured to start a launch's
+  // second CTA only once its first had allocated and given up the
+  // allocation permit (~3 us later in balanced mode, after the lengths'
+  // prefix sums).  A CTA that then leaves before the main body frees it.
+  if (early_tmem && warp == 5) {
+    tmem_alloc(tmem_slot, dec_tmem_cols<KV>());
+    tmem_relinquish();
+  }
+  auto leave_early = [&]() {
+    if (!early_tmem) return;
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+      tc_fence_after();
+      tmem_dealloc(*tmem_slot, dec_tmem_cols<KV>());
+    }
+  };
   griddep_wait();
   griddep_launch_dependents();
 
@@ -568,6 +586,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       float* orow = p.out + (long long)b * p.out_stride;
       for (long long i = fill_beg + 4 * tid; i < fill_end; i += 4 * kDecThreads)
         __stcs(reinterpret_cast<float4*>(orow + i), v4);
+      leave_early();
       return;
     }
     if (tid == 0) lens_s[0] = L;
@@ -701,11 +720,12 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         for (long long i = 4 * tid; i < n; i += 4 * kDecThreads)
           __stcs(reinterpret_cast<float4*>(dst + i), v4);
       });
+      leave_early();
       return;
     }
   }
 
-  if (warp == 5) {
+  if (!early_tmem && warp == 5) {
     tmem_alloc(tmem_slot, dec_tmem_cols<KV>());
     tmem_relinquish();
   }
@@ -1257,7 +1277,9 @@ static cudaError_t launch_decode_t(const RowsParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<KV, SEL>, kmap, qmap, p, G, balanced);
+  // more CTAs than SMs: take the tensor memory early (see the kernel)
+  const int early_tmem = (long long)cfg.gridDim.x * cfg.gridDim.y > sms ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<KV, SEL>, kmap, qmap, p, G, balanced, early_tmem);
 }
 
 // The balanced grid of the current device for keys of kv_dtype.

@@ -174,7 +174,6 @@ __global__ void __launch_bounds__(kMgThreads) topk_merge_kernel(const MergeParam
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.x;
   sm100::griddep_wait();
-  sm100::griddep_launch_dependents();
   const int k = p.k;
   int* oidx = p.idx + (long long)r * p.out_stride;
   float* oval = p.vals ? p.vals + (long long)r * p.out_stride : nullptr;
@@ -220,6 +219,9 @@ __global__ void __launch_bounds__(kMgThreads) topk_merge_kernel(const MergeParam
         }
       }
       __syncthreads();
+      // the next launch may start once the candidates are staged (its CTAs
+      // would otherwise take SM slots this grid's CTAs still wait for)
+      sm100::griddep_launch_dependents();
       merge_select(n, n, k, [](int) { return true; }, [&](int i) { return s_val[i]; },
                    [&](int i) { return s_pos[i]; }, oidx, oval, hist, scr);
       return;
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(kMgThreads) topk_merge_kernel(const MergeParam
   for (int s = tid; s < ns; s += kMgThreads) m += count_of(s);
   int n;
   mg_scan(m, scr, &n);
+  sm100::griddep_launch_dependents();
   merge_select(
       ns * k, n, k, [&](int f) { return f % k < count_of(f / k); },
       [&](int f) { return __ldg(slots + (f / k) * sf + kSlotHead + f % k); },

@@ -171,7 +171,6 @@ __global__ void __launch_bounds__(kTkThreads)
   const int crank = kCl > 1 ? (int)cg::this_cluster().block_rank() : 0;
   // the logits were written by the previous launch
   sm100::griddep_wait();
-  sm100::griddep_launch_dependents();
   const int Lraw = __ldg(p.seqlens + r);
   const bool bad = Lraw > p.T;
   const int L = bad ? 0 : max(Lraw, 0);
@@ -622,6 +621,10 @@ __global__ void __launch_bounds__(kTkThreads)
   __syncthreads();
 
   // ---- the selection, in position order
+  // Only now may the next launch start: its CTAs, started earlier, would
+  // take SM slots this grid's CTAs (most of an SM's shared memory each) are
+  // still waiting for (measured: 0.5-1.5 us per call with a decode next).
+  sm100::griddep_launch_dependents();
   int o = w_out[warp];
   const int o_end = o + w_gt[warp] + w_take[warp];
   const int o_lim = min(o_end, p.k);         // the counts say o_end <= k; never write past k

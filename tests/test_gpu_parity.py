@@ -209,29 +209,38 @@ def test_config4_bf16_full_size_all_rows():
 
 def config5_rows(n_sms: int) -> list[int]:
     """Rows of the full-size prefill to compare value by value: the first
-    and the last query of every 16th query tile, and of the query tiles
+    and the last query of every 8th query tile, and of the query tiles
     where each persistent CTA's slice of the (query tile, position tile)
-    item list starts and ends (the kernel splits the list evenly over one
-    CTA per SM, so these rows sit at every CTA's boundaries)."""
+    item list starts and ends.  The kernel gives each of its n_sms CTAs an
+    equal share of the list's cost (an item weighs 16, a query tile adds 32
+    and 1/20 per page of its rows' tail past its last position tile); CTA k
+    starts at the first item whose cost range begins at or after k/n_sms of
+    the total, which is recomputed here."""
     w = wl.cfg5()
     T = w.W * w.P
     L = np.where(w.seqlens > T, 0, np.clip(w.seqlens, 0, T)).astype(np.int64)
     n_qt = (w.R + 3) // 4
     lmax = np.array([L[4 * j: 4 * j + 4].max() for j in range(n_qt)])
-    tiles = (lmax + 127) // 128
-    cum = np.concatenate([[0], np.cumsum(tiles)])
+    nrow = np.array([min(4, w.R - 4 * j) for j in range(n_qt)])
+    nt = (lmax + 127) // 128
+    wt = np.where(nt > 0, 16 * nt + 32 + nrow * np.maximum(w.W - 2 * nt, 0) // 20, 0)
+    cum = np.concatenate([[0], np.cumsum(wt)])
     total = int(cum[-1])
+
+    def tile_rows(j):
+        return (4 * j, min(4 * j + 3, w.R - 1))
+
     rows = set()
-    for j in range(0, n_qt, 16):
-        rows.update((4 * j, min(4 * j + 3, w.R - 1)))
-    for k in range(n_sms):
-        a = k * total // n_sms
-        b = (k + 1) * total // n_sms - 1
-        if b < a:
+    for j in range(0, n_qt, 8):
+        rows.update(tile_rows(j))
+    for k in range(1, n_sms):
+        x = k * total // n_sms
+        j = int(np.searchsorted(cum, x, side="right") - 1)
+        if j >= n_qt:
             continue
-        for item in (a, b):
-            j = int(np.searchsorted(cum, item, side="right") - 1)
-            rows.update((4 * j, min(4 * j + 3, w.R - 1)))
+        rows.update(tile_rows(j))          # the CTA's first item is in tile j ...
+        if j > 0:
+            rows.update(tile_rows(j - 1))  # ... or is tile j's first, the previous CTA ending in j - 1
     rows.update((0, w.R - 1))
     return sorted(rows)
 
@@ -240,7 +249,7 @@ def test_config5_prefill_full_size_sampled_rows():
     import torch
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
     rows = config5_rows(n_sms)
-    assert len(rows) >= 256
+    assert len(rows) >= 512
     _sampled(wl.cfg5(), rows)
 
 
