@@ -551,6 +551,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   };
 
   Tiles tiles;
+  int early_ph[2] = {-1, -1};   // balanced mode: the first tile's table entries (producer lane 0)
   if (!balanced) {
     // ---------------------------------------------------------------- per-request
     const int b = blockIdx.y, c = blockIdx.x;
@@ -633,45 +634,55 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       // fall in [k * NW / R, (k + 1) * NW / R), a row's first unit weighing
       // 1 + Y.  bf16 keys (the query comes by TMA) and the fused top-k (its
       // slots follow the plain split) take Y = 0, the plain split.
-      const long long Rg = gridDim.x;
-      const long long Y = (KV == DSA_KV_FP8_E4M3 && !SEL)
-                              ? min(8ll, (long long)run_v / Rg / 3) : 0ll;
+      const int Rg = gridDim.x;
+      const int Y = (KV == DSA_KV_FP8_E4M3 && !SEL) ? min(8, run_v / Rg / 3) : 0;
       int n_rows = 0;
       for (int base = 0; base < B; base += 32) {
         const int j = base + lane;
         n_rows += __popc(__ballot_sync(0xffffffffu, j < B && Pv[j + 1] > Pv[j]));
       }
-      const long long NW = run_v + Y * n_rows;
-      for (int e = 0; e < 2; ++e) {
-        const long long x = (blockIdx.x + e) * NW / Rg;
-        int u = run_v, nb = 0;
-        bool found = false;
-        for (int base = 0; base < B && !found; base += 32) {
-          const int j = base + lane;
-          const int len = j < B ? Pv[j + 1] - Pv[j] : 0;
-          const int ne = len > 0 ? 1 : 0;
-          int incl = ne;
+      // the two slice ends k * NW / R and (k + 1) * NW / R, as c * q +
+      // (c * r) / R with NW = q * R + r (c * r < R * R), found in one pass
+      // over the rows; a row's count of non-empty rows before it comes from
+      // a ballot
+      const long long NW = run_v + (long long)Y * n_rows;
+      const long long q = NW / Rg;
+      const unsigned r = (unsigned)(NW - q * Rg);
+      long long xe[2];
+      int ue[2] = {run_v, run_v};
+      bool found[2] = {false, false};
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-          }
-          const long long pw = Pv[min(j, B)] + Y * (nb + incl - ne);   // the row's weighted start
-          const bool here = ne && x < pw + len + Y;
-          const unsigned hb = __ballot_sync(0xffffffffu, here);
+      for (int e = 0; e < 2; ++e) {
+        const unsigned c = blockIdx.x + e;
+        xe[e] = (long long)c * q + (long long)(c * r / (unsigned)Rg);
+      }
+      int nb = 0;
+      for (int base = 0; base < B && !(found[0] && found[1]); base += 32) {
+        const int j = base + lane;
+        const int len = j < B ? Pv[j + 1] - Pv[j] : 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, len > 0);
+        const int before = nb + __popc(bal & ((1u << lane) - 1u));
+        const long long pw = Pv[min(j, B)] + (long long)Y * before;   // the row's weighted start
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (found[e]) continue;                                     // warp-uniform
+          const unsigned hb = __ballot_sync(0xffffffffu, len > 0 && xe[e] < pw + len + Y);
           if (hb) {
             const int src = __ffs(hb) - 1;
             int uu = 0;
             if (lane == src) {
-              const long long i = x <= pw ? 0 : max(1ll, x - pw - Y);
+              const long long i = xe[e] <= pw ? 0 : max(1ll, xe[e] - pw - Y);
               uu = Pv[j] + (int)min(i, (long long)len);
             }
-            u = __shfl_sync(0xffffffffu, uu, src);
-            found = true;
+            ue[e] = __shfl_sync(0xffffffffu, uu, src);
+            found[e] = true;
           }
-          nb += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (lane == 0) slice_s[e] = u;
+        nb += __popc(bal);
+      }
+      if (lane == 0) {
+        slice_s[0] = ue[0];
+        slice_s[1] = ue[1];
       }
       if (SEL) {
         // fused top-k: exclusive prefix sums of the rows' chunk counts (the
@@ -700,13 +711,24 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       }
     }
     __syncthreads();
-    const long long R = gridDim.x, k = blockIdx.x;
-    const long long F = p.fill ? Pf[B] : 0;
+    // this CTA's fill pages [k * F / R, (k + 1) * F / R), as c * q + (c * r) / R
+    const unsigned R = gridDim.x, k = blockIdx.x;
+    const int F = p.fill ? Pf[B] : 0;
     const int u0 = slice_s[0], u1 = slice_s[1];
-    const int f0 = (int)(k * F / R), f1 = (int)((k + 1) * F / R);
+    const int fq = F / (int)R;
+    const unsigned fr = (unsigned)(F - fq * (int)R);
+    const int f0 = (int)k * fq + (int)(k * fr / R), f1 = (int)(k + 1) * fq + (int)((k + 1) * fr / R);
     if (u0 < u1) {
       tiles.init_balanced(Pv, B, u0, u1);
       if (KV == DSA_KV_FP8_E4M3 && tid < 128) q_load(tiles.row, q0raw, q0w);
+      if (KV == DSA_KV_FP8_E4M3 && tid == 128) {
+        // the producer's first tile: its table entries, read now (fp8 keys:
+        // measured 0.1 us faster on short slices; bf16 keys, whose first
+        // tile waits behind its query load anyway, measured 0.8 us slower)
+        const int* btrow = p.block_table + (long long)tiles.row * p.bt_stride;
+        early_ph[0] = __ldg(btrow + tiles.pg0);
+        if (tiles.pg1 >= 0) early_ph[1] = __ldg(btrow + tiles.pg1);
+      }
     }
 
     fill_f0 = f0;
@@ -868,7 +890,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
             const int pg = h == 0 ? it.pg0 : it.pg1;
             phys[h] = -1;
             if (pg >= 0) {
-              const int ph = __ldg(btrow + pg);
+              const int ph = (KV == DSA_KV_FP8_E4M3 && balanced && i == 0) ? early_ph[h]
+                                                                          : __ldg(btrow + pg);
               if (ph >= 0 && ph < p.num_pages) {
                 phys[h] = ph;
                 bytes += C::kPageBytes;
