@@ -767,8 +767,11 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     // ------------------------------------------------------------ TMA producer
     // The fill goes out as bulk copies from blocks of -inf / NaN in shared
     // memory.  Lanes 1-31 issue them all at once (copies from one thread
-    // complete one after another; from 31 they overlap) as soon as lane 0
-    // has issued its first stages' page loads.  bf16 keys, CTA with a long
+    // complete one after another; from 31 they overlap) once lane 0 has
+    // issued its last page loads: the page reads stream first, and the
+    // writes, absorbed by L2, drain while the last tiles are processed
+    // (config 3: 28.2 us, against 30.2 us when released after the first S
+    // tiles and 32.6 us at once).  bf16 keys, CTA with a long
     // page stream (16 pages or more): lane 0 issues them instead, in step
     // with its page loads, a share after every tile from the S-th on, so
     // that DRAM serves a steady mix of reads and writes (measured ~1% faster
@@ -786,7 +789,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       fence_proxy_async_smem();
       __syncwarp();
     }
-    // the first stages: after them (or after all tiles, if fewer) the fill may go
+    // this CTA's tiles; the paced fill starts after the first S of them
     const int n_tiles = max((my_pages + 1) / 2, 1);
     const int first_fill = min(S, n_tiles);
     constexpr bool kCanPace = KV == DSA_KV_BF16;
@@ -919,10 +922,10 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     };
     if (lane != 0) {
       if (burst) {
-        // wait (bounded: ~0.3 s) for lane 0's first stages, then issue this
-        // lane's chunks: chunk c of the CTA's share (4 KB, or 1 KB of NaN)
-        // goes to lane 1 + c % 31
-        for (int spin = 0; *tiles_out < first_fill && spin < (1 << 22); ++spin) __nanosleep(64);
+        // wait (bounded: ~0.5 s) for lane 0's last page loads, then issue
+        // this lane's chunks: chunk c of the CTA's share (4 KB, or 1 KB of
+        // NaN) goes to lane 1 + c % 31
+        for (int spin = 0; *tiles_out < n_tiles && spin < (1 << 22); ++spin) __nanosleep(128);
         int c = 0;
         bool any = false;
         for_each_fill_range(lane == 1, [&](float* dst, long long n, bool bad) {
