@@ -629,13 +629,13 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       __syncwarp();
       // fp8 keys: this CTA's pages [u0, u1) balance pages plus a weight Y
       // per row start (a row segment's query is loaded and split by the
-      // CTA itself), Y = min(8, pages per CTA / 3) so that short slices are
+      // CTA itself), Y = min(6, pages per CTA / 4) so that short slices are
       // not swamped by it; each CTA takes the units whose weighted starts
       // fall in [k * NW / R, (k + 1) * NW / R), a row's first unit weighing
       // 1 + Y.  bf16 keys (the query comes by TMA) and the fused top-k (its
       // slots follow the plain split) take Y = 0, the plain split.
       const int Rg = gridDim.x;
-      const int Y = (KV == DSA_KV_FP8_E4M3 && !SEL) ? min(8, run_v / Rg / 3) : 0;
+      const int Y = (KV == DSA_KV_FP8_E4M3 && !SEL) ? min(6, run_v / Rg / 4) : 0;
       int n_rows = 0;
       for (int base = 0; base < B; base += 32) {
         const int j = base + lane;

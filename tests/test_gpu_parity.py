@@ -369,6 +369,30 @@ def test_back_to_back_calls_into_one_output(kind):
     compare(out.cpu().numpy(), oracle_rows(b)[0])
 
 
+@pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
+def test_more_ctas_than_sms_with_idle_ctas(kv):
+    """Per-request mode with more CTAs than SMs (64 rows of a 32-page table:
+    four CTAs a row, so the CTAs take their tensor memory before waiting for
+    the previous launch) and rows short enough that some CTAs have no page
+    and leave early; two calls back to back into one output, so that each
+    launch's CTAs start while the previous launch runs."""
+    import torch
+    g = np.random.default_rng(21)
+    lengths = [int(x) for x in g.integers(0, 32 * 64 + 1, 64)]
+    lengths[:8] = [0, 1, 63, 64, 65, 127, 2048, -3]
+    a = wl.decode_with_lengths("early_a", lengths, 32, seed=21, kv_dtype=kv)
+    b = wl.decode_with_lengths("early_b", [max(0, x // 3) for x in lengths], 32, seed=21,
+                               kv_dtype=kv)
+    _check_full(a)
+    da, db = DeviceWorkload(a), DeviceWorkload(b)
+    out = torch.empty_like(da.out)
+    for _ in range(3):
+        assert da.call(out=out) == 0
+        assert db.call(out=out) == 0
+    torch.cuda.synchronize()
+    compare(out.cpu().numpy(), oracle_rows(b)[0])
+
+
 # --- long tables: CTAs are dispatched longest row first -----------------------
 
 @pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
