@@ -1224,18 +1224,16 @@ bool decode_is_balanced(int W, int rows) { return W > 64 && rows <= kMaxRowsBala
 
 // CTAs per request in per-request mode, from the launch shape only: at most
 // the per-dtype cap and W.  For a short table (W <= 64 pages, so no request
-// is long) about one CTA per SM in total: each CTA pipelines a few pages
-// instead of paying its start-up latency for one, and the next launch's
-// CTAs find room to start (programmatic dependent launch) while this one
-// runs.  Two per SM when a CTA would otherwise hold more than 8 pages.
-// (Measured: B=16/32 rows 5.5 us per launch at one per SM, 6.0 at two; 64
-// rows of 32 pages 8.6 us at two, 9.9 at one.)
+// is long) about two CTAs per SM in total, the resident limit: each CTA
+// pipelines a few pages instead of paying its start-up latency for one.
+// (Measured: B=16/32 rows 5.3 / 5.4 us per launch at two per SM, 5.8 at one;
+// before the tensor memory was taken ahead of the dependent-launch wait, an
+// SM started its second CTA ~1.4 us late and one per SM was faster.)
 template <int KV>
 int decode_slots(int W, int B, int sms) {
   int G = W < DecCfg<KV>::kMaxSlots ? W : DecCfg<KV>::kMaxSlots;
   if (W <= 64) {
-    int g = sms / B > 1 ? sms / B : 1;
-    if ((W + g - 1) / g > 8) g = 2 * sms / B > 1 ? 2 * sms / B : 1;
+    const int g = 2 * sms / B > 1 ? 2 * sms / B : 1;
     if (G > g) G = g;
   }
   return G < 1 ? 1 : G;
