@@ -18,11 +18,13 @@
 //    and exits.  G is capped so that the few pages of a short table are
 //    pipelined by one CTA instead of each paying a CTA's start-up latency.
 //  * balanced (long tables): one persistent CTA per resident slot; the valid
-//    (request, page) pairs of all rows, in row order, are split into equal
-//    contiguous slices (prefix sums of the rows' valid page counts, computed
-//    by every CTA), and the positions past each length are split the same
-//    way.  No CTA is the tail of a long request.  A slice can cross rows; the
-//    query operand is double-buffered per row segment.
+//    (request, page) pairs of all rows, in row order, are split into
+//    contiguous slices of equal cost (prefix sums of the rows' valid page
+//    counts, computed by every CTA; with fp8 keys a row start costs a few
+//    pages more, as the CTA splits that row's query itself), and the
+//    positions past each length are split evenly.  No CTA is the tail of a
+//    long request.  A slice can cross rows; the query operand is
+//    double-buffered per row segment.
 //
 // Per valid page pair (a 128-position tile):
 //   TMA      page rows -> shared memory (128-byte swizzle), no gathered copy
