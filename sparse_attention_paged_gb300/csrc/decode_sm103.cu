@@ -864,62 +864,62 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       constexpr bool kPaced = decltype(paced_c)::value;
       Tiles it = tiles;
       for (int i = 0; it.valid(); ++i, it.next()) {
-          if (KV == DSA_KV_BF16 && it.seg != seg_loaded) {
-            // query of this row segment -> buffer seg % 2, once segment seg-2
-            // (the buffer's previous user) has finished its MMAs
-            const int sb = it.seg & 1;
-            if (it.seg >= 2) ok = mbar_wait_bounded(&bempty[sb], ((it.seg - 2) >> 1) & 1, kWaitLimit);
-            if (!ok) break;
-            mbar_arrive_expect_tx(&qbar[sb], C::kQBytes);
-            tma_load_2d(sQ + sb * C::kQBytes, &qmap, &qbar[sb], 0, it.row * kHeads);
-            tma_load_2d(sQ + sb * C::kQBytes + C::kQBytes / 2, &qmap, &qbar[sb], kHalfRowUnits,
-                        it.row * kHeads);
-            seg_loaded = it.seg;
-          }
-          const int s = i % S;
-          if (i >= S) ok = mbar_wait_bounded(&empty[s], ((i / S) - 1) & 1, kWaitLimit);
-          if (!ok || *abort_flag) break;
+        if (KV == DSA_KV_BF16 && it.seg != seg_loaded) {
+          // query of this row segment -> buffer seg % 2, once segment seg-2
+          // (the buffer's previous user) has finished its MMAs
+          const int sb = it.seg & 1;
+          if (it.seg >= 2) ok = mbar_wait_bounded(&bempty[sb], ((it.seg - 2) >> 1) & 1, kWaitLimit);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&qbar[sb], C::kQBytes);
+          tma_load_2d(sQ + sb * C::kQBytes, &qmap, &qbar[sb], 0, it.row * kHeads);
+          tma_load_2d(sQ + sb * C::kQBytes + C::kQBytes / 2, &qmap, &qbar[sb], kHalfRowUnits,
+                      it.row * kHeads);
+          seg_loaded = it.seg;
+        }
+        const int s = i % S;
+        if (i >= S) ok = mbar_wait_bounded(&empty[s], ((i / S) - 1) & 1, kWaitLimit);
+        if (!ok || *abort_flag) break;
 #ifdef DSA_TEST_SKIP_FIRST_TILE
-          // test builds only: never deliver the first tile, so that the MMA's
-          // bounded wait for it runs out and the call reports DSA_ERR_TIMEOUT
-          if (i == 0) {
-            issued = i + 1;
-            continue;
-          }
-#endif
-          const int* btrow = p.block_table + (long long)it.row * p.bt_stride;
-          int phys[2];
-          uint32_t bytes = 0;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int pg = h == 0 ? it.pg0 : it.pg1;
-            phys[h] = -1;
-            if (pg >= 0) {
-              const int ph = (KV == DSA_KV_FP8_E4M3 && balanced && i == 0) ? early_ph[h]
-                                                                          : __ldg(btrow + pg);
-              if (ph >= 0 && ph < p.num_pages) {
-                phys[h] = ph;
-                bytes += C::kPageBytes;
-              }
-            }
-          }
-          mbar_arrive_expect_tx(&full[s], bytes);
-          uint8_t* st = sA + s * C::kTileBytes;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (phys[h] < 0) continue;
-            if (KV == DSA_KV_FP8_E4M3) {
-              tma_load_3d(st + h * C::kPageBytes, &kmap, &full[s], 0, 0, phys[h]);
-            } else {
-              // K-block 0 (d 0..63) and K-block 1 (d 64..127), rows of 128 B
-              tma_load_3d(st + h * (C::kPageBytes / 2), &kmap, &full[s], 0, 0, phys[h]);
-              tma_load_3d(st + C::kTileBytes / 2 + h * (C::kPageBytes / 2), &kmap, &full[s],
-                          kHalfRowUnits, 0, phys[h]);
-            }
-          }
+        // test builds only: never deliver the first tile, so that the MMA's
+        // bounded wait for it runs out and the call reports DSA_ERR_TIMEOUT
+        if (i == 0) {
           issued = i + 1;
-          *tiles_out = i + 1;
-          if (kPaced && i + 1 >= first_fill) issue_fill(per_page * (it.pg1 >= 0 ? 2 : 1));
+          continue;
+        }
+#endif
+        const int* btrow = p.block_table + (long long)it.row * p.bt_stride;
+        int phys[2];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int pg = h == 0 ? it.pg0 : it.pg1;
+          phys[h] = -1;
+          if (pg >= 0) {
+            const int ph = (KV == DSA_KV_FP8_E4M3 && balanced && i == 0) ? early_ph[h]
+                                                                        : __ldg(btrow + pg);
+            if (ph >= 0 && ph < p.num_pages) {
+              phys[h] = ph;
+              bytes += C::kPageBytes;
+            }
+          }
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        uint8_t* st = sA + s * C::kTileBytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (phys[h] < 0) continue;
+          if (KV == DSA_KV_FP8_E4M3) {
+            tma_load_3d(st + h * C::kPageBytes, &kmap, &full[s], 0, 0, phys[h]);
+          } else {
+            // K-block 0 (d 0..63) and K-block 1 (d 64..127), rows of 128 B
+            tma_load_3d(st + h * (C::kPageBytes / 2), &kmap, &full[s], 0, 0, phys[h]);
+            tma_load_3d(st + C::kTileBytes / 2 + h * (C::kPageBytes / 2), &kmap, &full[s],
+                        kHalfRowUnits, 0, phys[h]);
+          }
+        }
+        issued = i + 1;
+        *tiles_out = i + 1;
+        if (kPaced && i + 1 >= first_fill) issue_fill(per_page * (it.pg1 >= 0 ? 2 : 1));
       }
     };
     if (lane != 0) {
