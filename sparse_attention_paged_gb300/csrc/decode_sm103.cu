@@ -450,6 +450,16 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     tmem_alloc(tmem_slot, dec_tmem_cols<KV>());
     tmem_relinquish();
   }
+  // the blocks of -inf / NaN the balanced mode's fill is copied from (the
+  // logits instance; written before the wait, as they read no input)
+  if (!SEL && warp == 4 && balanced) {
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    const float4 qnan = make_float4(nanf_(), nanf_(), nanf_(), nanf_());
+    for (int j = lane; j < kFillBlock / 16; j += 32) reinterpret_cast<float4*>(sInf)[j] = ninf;
+    for (int j = lane; j < kNanBlock / 16; j += 32) reinterpret_cast<float4*>(sNan)[j] = qnan;
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
   auto leave_early = [&]() {
     if (!early_tmem) return;
     tc_fence_before();
@@ -783,14 +793,6 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     // warp issuing the burst between lane 0's first and later stages, was
     // also slower.)
     const bool any_fill = balanced ? fill_f0 < fill_f1 : fill_end > fill_beg;
-    if (any_fill) {
-      const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      const float4 qnan = make_float4(nanf_(), nanf_(), nanf_(), nanf_());
-      for (int j = lane; j < kFillBlock / 16; j += 32) reinterpret_cast<float4*>(sInf)[j] = ninf;
-      for (int j = lane; j < kNanBlock / 16; j += 32) reinterpret_cast<float4*>(sNan)[j] = qnan;
-      fence_proxy_async_smem();
-      __syncwarp();
-    }
     // this CTA's tiles; the paced fill starts after the first S of them
     const int n_tiles = max((my_pages + 1) / 2, 1);
     const int first_fill = min(S, n_tiles);
