@@ -611,12 +611,14 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     for (int j = tid; j < B; j += kDecThreads) lens_s[j] = __ldg(p.seqlens + j);
     __syncthreads();
     if (warp == 0) {
-      // exclusive prefix sums of valid pages and of fill pages (W - valid)
-      int run_v = 0, run_f = 0;
+      // exclusive prefix sums of valid pages and of fill pages (W - valid),
+      // and the count of non-empty rows
+      int run_v = 0, run_f = 0, n_rows = 0;
       for (int base = 0; base < B; base += 32) {
         const int j = base + lane;
         const int v = j < B ? valid_pages(lens_s[j], p.W) : 0;
         const int f = j < B ? p.W - v : 0;
+        n_rows += __popc(__ballot_sync(0xffffffffu, v > 0));
         int sv = v, sf = f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -648,18 +650,21 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       // slots follow the plain split) take Y = 0, the plain split.
       const int Rg = gridDim.x;
       const int Y = (KV == DSA_KV_FP8_E4M3 && !SEL) ? min(6, run_v / Rg / 4) : 0;
-      int n_rows = 0;
-      for (int base = 0; base < B; base += 32) {
-        const int j = base + lane;
-        n_rows += __popc(__ballot_sync(0xffffffffu, j < B && Pv[j + 1] > Pv[j]));
-      }
       // the two slice ends k * NW / R and (k + 1) * NW / R, as c * q +
       // (c * r) / R with NW = q * R + r (c * r < R * R), found in one pass
       // over the rows; a row's count of non-empty rows before it comes from
       // a ballot
       const long long NW = run_v + (long long)Y * n_rows;
-      const long long q = NW / Rg;
-      const unsigned r = (unsigned)(NW - q * Rg);
+      long long q;
+      unsigned r;
+      if (NW < (1ll << 31)) {            // the usual case: a 32-bit division
+        const unsigned nw = (unsigned)NW, q32 = nw / (unsigned)Rg;
+        q = q32;
+        r = nw - q32 * (unsigned)Rg;
+      } else {
+        q = NW / Rg;
+        r = (unsigned)(NW - q * Rg);
+      }
       long long xe[2];
       int ue[2] = {run_v, run_v};
       bool found[2] = {false, false};
