@@ -611,34 +611,29 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     for (int j = tid; j < B; j += kDecThreads) lens_s[j] = __ldg(p.seqlens + j);
     __syncthreads();
     if (warp == 0) {
-      // exclusive prefix sums of valid pages and of fill pages (W - valid),
-      // and the count of non-empty rows
-      int run_v = 0, run_f = 0, n_rows = 0;
+      // exclusive prefix sums of valid pages, and the count of non-empty
+      // rows; a row's fill pages are W minus its valid pages, so their
+      // prefix sums follow: Pf[j] = j * W - Pv[j]
+      int run_v = 0, n_rows = 0;
       for (int base = 0; base < B; base += 32) {
         const int j = base + lane;
         const int v = j < B ? valid_pages(lens_s[j], p.W) : 0;
-        const int f = j < B ? p.W - v : 0;
         n_rows += __popc(__ballot_sync(0xffffffffu, v > 0));
-        int sv = v, sf = f;
+        int sv = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int tv = __shfl_up_sync(0xffffffffu, sv, o);
-          const int tf = __shfl_up_sync(0xffffffffu, sf, o);
-          if (lane >= o) {
-            sv += tv;
-            sf += tf;
-          }
+          if (lane >= o) sv += tv;
         }
         if (j < B) {
           Pv[j] = run_v + sv - v;
-          Pf[j] = run_f + sf - f;
+          Pf[j] = (int)((long long)j * p.W - (run_v + sv - v));
         }
         run_v += __shfl_sync(0xffffffffu, sv, 31);
-        run_f += __shfl_sync(0xffffffffu, sf, 31);
       }
       if (lane == 0) {
         Pv[B] = run_v;
-        Pf[B] = run_f;
+        Pf[B] = (int)((long long)B * p.W - run_v);
       }
       __syncwarp();
       // fp8 keys: this CTA's pages [u0, u1) balance pages plus a weight Y
