@@ -44,7 +44,7 @@
  *             The library allocates nothing, never synchronises and
  *             launches one kernel per call on `stream` (a cudaStream_t;
  *             NULL = legacy default stream); the top-k calls launch two, the
- *             varlen prefill one per request.  All calls are legal inside
+ *             varlen prefill one per 128 requests.  All calls are legal inside
  *             stream capture.  Every kernel is launched with
  *             programmatic dependent launch allowed: its set-up may overlap
  *             the tail of the previous kernel in the stream, but it reads no
@@ -161,13 +161,14 @@ int dsa_indexer_logits_prefill(const void* q, const float* w,
  *
  * cu_q is a HOST array of n_req + 1 offsets: cu_q[0] = 0, non-decreasing
  * (DSA_ERR_INVALID_ARG otherwise, checked before any launch); n_q =
- * cu_q[n_req] rows in all.  Each non-empty request runs the query-tile
- * kernel of dsa_indexer_logits_prefill (one launch each, in request order,
- * on `stream`), so requests of many tokens reuse each key tile four times;
- * requests of one or a few tokens are better served by per-query rows.
- * Other arguments, layouts, alignment, range and device errors as for
- * dsa_indexer_logits_prefill.  DSA_ERR_CUDA from a launch may leave the
- * earlier requests launched.
+ * cu_q[n_req] rows in all.  The requests' query tiles run in one launch of
+ * the query-tile kernel of dsa_indexer_logits_prefill (up to 128 requests a
+ * launch; more run as further launches, in request order, on `stream`),
+ * each tile reading its own request's table row, so requests of many tokens
+ * reuse each key tile four times; requests of one or a few tokens are
+ * better served by per-query rows.  Other arguments, layouts, alignment,
+ * range and device errors as for dsa_indexer_logits_prefill.  DSA_ERR_CUDA
+ * from a launch may leave the earlier groups of requests launched.
  */
 int dsa_indexer_logits_prefill_varlen(const void* q, const float* w, const void* kcache,
                                       const void* kscale, long long page_stride_bytes,
