@@ -254,6 +254,9 @@ def job_throughput(world: int, steps: int, units_per_step: int, elapsed_ms: floa
 # ---------------------------------------------------------------------------
 # our arm
 
+VARLEN_REQUESTS_PER_LAUNCH = 128    # the library's request map per varlen launch
+
+
 class DeviceCall:
     """One library call with device-resident inputs and its own output."""
 
@@ -306,7 +309,11 @@ class DeviceCall:
         if self.w.kind == "topk":
             return 2
         if self.cu_q is not None:
-            return sum(1 for a, b in zip(self.cu_q, self.cu_q[1:]) if b > a)
+            # the varlen prefill: one launch per group of up to
+            # VARLEN_REQUESTS_PER_LAUNCH requests that holds any row
+            c, n = list(self.cu_q), len(self.cu_q) - 1
+            g = VARLEN_REQUESTS_PER_LAUNCH
+            return sum(1 for b0 in range(0, n, g) if c[min(b0 + g, n)] > c[b0])
         return 1
 
     def nbytes(self):

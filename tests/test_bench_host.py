@@ -24,13 +24,29 @@ def test_call_objects(name):
         elif w.meta.get("varlen"):
             cu = c.cu_q
             assert cu[0] == 0 and cu[-1] == w.R
-            assert n == sum(1 for a, b in zip(cu, cu[1:]) if b > a)
+            # one launch per group of up to 128 requests holding any row
+            groups = [(b0, min(b0 + 128, len(cu) - 1)) for b0 in range(0, len(cu) - 1, 128)]
+            assert n == sum(1 for a, b in groups if cu[b] > cu[a])
             assert c.host_table().shape == (len(cu) - 1, w.W)
         else:
             assert n == 1
         if w.kind != "store":
             assert c.host_table().shape[1] == w.W
         assert c.nbytes() > 0
+
+
+def test_varlen_launch_count():
+    """The varlen prefill launches once per group of up to 128 requests that
+    holds any row: 4 requests -> 1, 131 -> 2, an empty group -> none."""
+    class C:
+        pass
+    for cu, want in (([0, 5, 9, 9, 20], 1), (list(range(132)), 2),
+                     ([0] * 129 + [1, 2, 3], 1), ([0, 0, 0], 0)):
+        c = bench.DeviceCall.__new__(bench.DeviceCall)
+        c.w = C()
+        c.w.kind = "prefill"
+        c.cu_q = cu
+        assert c.launches() == want, (cu[:5], want)
 
 
 def test_sweep_covers_every_configuration():
