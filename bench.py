@@ -59,8 +59,8 @@ WORKLOAD_DESC = {
     "5": "prefill bf16 n_q=4096 W=352 causal limit 18432+i",
     "6": "prefill bf16, 4 requests (query tokens, context) = (256, 6144), (512, 12288), "
          "(128, 3072), (1024, 20480), per-query table rows",
-    "6v": "prefill bf16, the same 4 requests, one table row per request (a query-tile launch "
-          "per request)",
+    "6v": "prefill bf16, the same 4 requests, one table row per request (all requests' query "
+          "tiles in one launch)",
     "7": "prefill fp8 n_q=1024 W=128 causal limit 7168+i",
     "8": "key-cache store: 65536 bf16 key rows into e4m3 pages (+ scales), random slots of 2048 pages",
     "9": "decode fp8 B=64 W=4097 L log-uniform 512..32768, top-2048 positions per request",

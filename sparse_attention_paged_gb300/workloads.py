@@ -466,7 +466,7 @@ def cfg6() -> Workload:
 
 def cfg6v() -> Workload:
     """Config 6's four requests called with one block-table row per request
-    and the request offsets: one query-tile launch per request."""
+    and the request offsets: all requests' query tiles in one launch."""
     w = cfg6()
     w.name = "prefill_bf16_varlen4_q1920_reqrows"
     w.meta["varlen"] = True
