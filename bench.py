@@ -489,6 +489,9 @@ def config_record(name, w, us, launches, region_ms, n_copies, resident, peaks, c
            "avg_launch_us": us, "launches": launches, "region_ms": region_ms,
            "positions_per_s": w.valid_positions / (us / 1e6)}
     rec.update(roofline_record(w, us, peaks))
+    # ncu DRAM bytes per launch, where profiles/dram_traffic.json holds them
+    # for the current kernel sources (else None)
+    rec["traffic"] = recorded_traffic(w.kind, w.name)
     rec["l2"] = (f"rotates over {n_copies} copies ({resident / 2**20:.0f} MiB resident)")
     rec["clocks"] = clocks
     return rec

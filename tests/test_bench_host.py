@@ -95,3 +95,13 @@ def test_roofline_record_bounds():
     r = bench.roofline_record(w5, us, peaks)
     assert r["bound"] == "tensor" and abs(r["frac"] - 0.75) < 1e-9
     assert abs(r["frac_sustained"] - 0.75 * 2000 / 1700) < 1e-9
+
+
+def test_config_record_carries_recorded_traffic():
+    """A per-configuration record reports the ncu DRAM bytes recorded for
+    its kernel, or None where none match the current sources."""
+    w = wl.NAMED["3"]()[0]
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1700.0}
+    rec = bench.config_record("3", w, 30.0, 100, 3.0, 4, 2**30, peaks, {})
+    assert "traffic" in rec
+    assert rec["traffic"] == bench.recorded_traffic(w.kind, w.name)
