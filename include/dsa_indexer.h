@@ -207,7 +207,9 @@ typedef enum {
  *     chunk of up to 32 pages of a row, and writes each chunk's best
  *     min(k_top, n) positions with their logits to the workspace; a merge
  *     kernel then selects each request's best among them.  No logit of the
- *     call is written to global memory.  It applies when k_top <= 1024, the
+ *     call is written to global memory.  It applies when k_top <= 2048 (a
+ *     chunk: for k_top >= 2048 every chunk keeps all its positions and the
+ *     merge does all the selecting), the
  *     decode takes its balanced form (W > 64 and B <= 384) and the
  *     workspace holds 4 * ceil((B + 1) / 4) + (C + B + ceil(B * W / 32)) *
  *     (4 + 2 * k_top) floats, C being the decode's persistent CTAs (two per

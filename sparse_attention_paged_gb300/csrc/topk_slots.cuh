@@ -25,7 +25,7 @@ namespace dsa {
 
 constexpr int kSelChunkPages = 32;                 // pages per chunk
 constexpr int kSelChunk = kSelChunkPages * kPage;  // 2,048 positions
-constexpr int kSelMaxK = kSelChunk / 2;            // the fused form's largest k
+constexpr int kSelMaxK = kSelChunk;                // the fused form's largest k (a chunk)
 constexpr int kSlotHead = 4;                       // floats before a slot's logits
 
 __host__ __device__ __forceinline__ long long sel_slot_floats(int k) {

@@ -201,7 +201,7 @@ def _same_as_two_pass(w, k, expect_status=0):
 
 
 @pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
-@pytest.mark.parametrize("k", [1, 64, 300, 1024])
+@pytest.mark.parametrize("k", [1, 64, 300, 1024, 2048])
 def test_topk_fused_matches_two_pass(kv, k):
     """Rows shorter than k, of exactly k, crossing several 2,048-position
     chunks, and the whole table; a ragged last page."""
@@ -252,9 +252,9 @@ def test_topk_fused_refused_where_it_does_not_apply():
     w = wl.decode_with_lengths("tkf_short", [100, 2000], 40, seed=62)
     st, idx, _, _ = _topk_form(w, 64, lib.TOPK_FUSED, _fused_ws_floats(2, 40, 64))
     assert st == 2 and (idx == -7).all()
-    # k above half a chunk
+    # k above a chunk
     w = wl.decode_with_lengths("tkf_bigk", [100, 9000], 150, seed=63)
-    st, _, _, _ = _topk_form(w, 1025, lib.TOPK_FUSED, _fused_ws_floats(2, 150, 1025))
+    st, _, _, _ = _topk_form(w, 2049, lib.TOPK_FUSED, _fused_ws_floats(2, 150, 2049))
     assert st == 2
     # a workspace too small for the slots
     st, _, _, _ = _topk_form(w, 512, lib.TOPK_FUSED)
