@@ -137,6 +137,26 @@ def test_length_past_table_is_a_nan_row():
     compare(o, ref)
 
 
+@pytest.mark.parametrize("kv,W,lengths", [
+    (wl.KV_E4M3, 90, [5000, 90 * 64 + 1, 3000, 0, 90 * 64, 64, 65]),
+    (wl.KV_BF16, 2048, [2048 * 64, 2048 * 64 + 1, 100000, 70000, 2048 * 64]),
+], ids=["fp8_fill_lanes", "bf16_paced_fill"])
+def test_balanced_length_past_table_is_a_nan_row(kv, W, lengths):
+    """Long tables (the balanced split) with a row longer than the table:
+    that whole row is NaN, written by the fill's bulk copies from the NaN
+    block, and the call reports status 7; every other row is exact.  The
+    bf16 case holds about 22 pages per CTA, so its fill goes out paced from
+    the producer's lane 0; the fp8 case goes through the 31 fill lanes."""
+    w = wl.decode_with_lengths(f"bal_badlen_{W}", lengths, W, seed=70, kv_dtype=kv)
+    dw = _run(w)
+    assert int(dw.status.item()) == 7
+    ref, st = oracle_rows(w)
+    assert st == 7
+    o = dw.out.cpu().numpy()
+    assert np.isnan(o[1]).all()
+    compare(o, ref)
+
+
 # --- CUDA graph capture: fixed grid, data-dependent work --------------------
 
 def test_graph_capture_and_replay_with_new_lengths():
