@@ -126,6 +126,27 @@ def test_bad_page_id_poisons_its_positions():
     compare(dw.out.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
+def test_balanced_bad_page_ids(kv):
+    """Long tables (the balanced split): every fifth table entry of two rows
+    lies outside the pool (some are the first page of a CTA's slice, whose
+    entries the fp8 path reads ahead) and one is negative; their positions
+    are NaN, the call reports status 6, and every other position is
+    exact."""
+    W = 90
+    w = wl.decode_with_lengths("bal_badpage", [5000, 3000, W * 64, 700, 64], W, seed=71,
+                               kv_dtype=kv)
+    w.block_table = w.block_table.copy()
+    w.block_table[0, ::5] = w.num_pages + 3
+    w.block_table[2, 2::5] = w.num_pages + 100
+    w.block_table[3, 4] = -1
+    dw = _run(w)
+    assert int(dw.status.item()) == 6
+    ref, st = oracle_rows(w)
+    assert st == 6
+    compare(dw.out.cpu().numpy(), ref)
+
+
 def test_length_past_table_is_a_nan_row():
     w = wl.decode_with_lengths("badlen", [100, 3 * 64 + 1, 5], 3, seed=6)
     dw = _run(w)
@@ -420,6 +441,17 @@ def test_longest_first_order_with_ties(kv):
     W = 70
     lengths = [500, 4000, 500, 4000, 0, W * 64, 1, 4000, -2, 64]
     _check_full(wl.decode_with_lengths("ties", lengths, W, seed=12, kv_dtype=kv))
+
+
+@pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
+def test_balanced_with_the_most_rows(kv):
+    """384 rows over a 65-page table, the most rows the balanced split takes
+    (its per-row prefix sums live in shared memory): twelve 32-row chunks in
+    the prefix sums and the slice search, rows of every length."""
+    g = np.random.default_rng(14)
+    lengths = g.integers(0, 65 * 64 + 1, 384)
+    lengths[:6] = [0, 1, 64, 65, 65 * 64, 2]
+    _check_full(wl.decode_with_lengths("most_rows", lengths, 65, seed=14, kv_dtype=kv))
 
 
 def test_many_rows_long_table_natural_order():
