@@ -213,6 +213,20 @@ def test_topk_fused_matches_two_pass(kv, k):
     _check(w, k, idx, val, list(range(w.R)))
 
 
+def test_topk_many_rows_both_forms():
+    """300 requests over a 70-page table: the two-pass selection runs one CTA
+    per request (2 * B CTAs no longer fit in one wave), the fused form's
+    slot header holds 300 rows; both forms agree bit for bit and the
+    selection is a valid top-k of the oracle's logits."""
+    g = np.random.default_rng(65)
+    lens = [int(x) for x in g.integers(0, 70 * 64 + 1, 300)]
+    lens[:5] = [0, 1, 64, 70 * 64, 130]
+    k = 128
+    w = wl.decode_with_lengths("tk_many", lens, 70, seed=65)
+    idx, val = _same_as_two_pass(w, k)
+    _check(w, k, idx, val, [0, 1, 2, 3, 4, 57, 150, 299])
+
+
 def test_topk_fused_ties_bad_pages_and_long_rows():
     """Tied logits (an all-zero query, zeroed pages), a page id outside the
     pool (NaN logits, status 6) and an over-long row (status 7): both forms
