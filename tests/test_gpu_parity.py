@@ -434,6 +434,27 @@ def test_more_ctas_than_sms_with_idle_ctas(kv):
     compare(out.cpu().numpy(), oracle_rows(b)[0])
 
 
+def test_concurrent_calls_on_three_streams():
+    """Three calls issued repeatedly on three streams at once: an fp8 and a
+    bf16 decode over long tables (two CTAs per SM each, tensor memory taken
+    before the dependent-launch wait, so CTAs of different calls share SMs)
+    and a per-request fp8 decode; every output stays exact."""
+    import torch
+    a = wl.decode_with_lengths("cc_a", [4400, 3000, 70 * 64, 100], 70, seed=80)
+    b = wl.decode_with_lengths("cc_b", [4000, 64, 1, 70 * 64], 70, seed=81, kv_dtype=wl.KV_BF16)
+    c = wl.decode_uniform("cc_c", 32, 16, 1024, 512, seed=82)
+    ds = [DeviceWorkload(x) for x in (a, b, c)]
+    streams = [torch.cuda.Stream() for _ in ds]
+    torch.cuda.synchronize()
+    for _ in range(20):
+        for d, st in zip(ds, streams):
+            assert d.call(stream=st.cuda_stream) == 0
+    torch.cuda.synchronize()
+    for x, d in zip((a, b, c), ds):
+        assert int(d.status.item()) == 0
+        compare(d.out.cpu().numpy(), oracle_rows(x)[0])
+
+
 # --- long tables: CTAs are dispatched longest row first -----------------------
 
 @pytest.mark.parametrize("kv", [wl.KV_E4M3, wl.KV_BF16])
